@@ -1,0 +1,204 @@
+"""ctypes binding of the C ABI in include/vc.h.
+
+Argument marshalling only: torch tensors in, device pointers and the current
+CUDA stream out to libvc.so.  Every step of the collectives runs in the CUDA
+kernels; if the library is missing, importing this module succeeds but every
+call raises (there is no CPU fallback).
+
+The tensor-level checks mirror PyTorch's capacity check before a collective
+("NCCL 专家课程 07", 源码五: the input must hold world_size times the output
+for ReduceScatter) and raise ValueError before anything reaches the library;
+the library repeats its own pointer-level checks.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Sequence
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_lib" / "libvc.so"
+
+DTYPES = {"int32": 0, "int64": 1, "float32": 2, "bfloat16": 3}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
+ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2}
+STATUS = {0: "VC_SUCCESS", 1: "VC_ERR_INVALID_ARGUMENT", 2: "VC_ERR_UNSUPPORTED",
+          3: "VC_ERR_ALIAS", 4: "VC_ERR_CUDA"}
+MAX_RANKS = 64
+
+# Every function the header declares (checked by the tests against vc.h).
+EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
+           "vc_all_reduce_decomposed", "vc_status_string")
+
+
+class VcError(RuntimeError):
+    """A non-zero vc_status_t from the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libvc.so with its prototypes set; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(
+                f"CUDA library missing ({LIB_PATH}); build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(str(LIB_PATH))
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        i32, sz, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+        L.vc_shard_count.argtypes = [sz, i32]
+        L.vc_shard_count.restype = sz
+        L.vc_reduce_scatter.argtypes = [vpp, vpp, i32, sz, i32, i32, i32, vp]
+        L.vc_all_gather.argtypes = [vpp, vpp, i32, sz, i32, vp]
+        L.vc_all_reduce.argtypes = [vpp, vpp, i32, sz, i32, i32, i32, vp]
+        L.vc_all_reduce_decomposed.argtypes = [vpp, vpp, vpp, i32, sz, i32, i32, i32, vp]
+        for f in ("vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
+                  "vc_all_reduce_decomposed"):
+            getattr(L, f).restype = i32
+        L.vc_status_string.argtypes = [i32]
+        L.vc_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def pointer_table(ptrs: Sequence[int]):
+    """A C array of device pointers (ints) as void**."""
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+
+
+def check_status(status: int):
+    if status != 0:
+        msg = lib().vc_status_string(status).decode()
+        raise VcError(status, msg)
+
+
+# ------------------------------------------------------------ tensor layer --
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_name(t) -> str:
+    torch = _torch()
+    names = {torch.int32: "int32", torch.int64: "int64", torch.float32: "float32",
+             torch.bfloat16: "bfloat16"}
+    if t.dtype not in names:
+        raise TypeError(f"unsupported dtype {t.dtype}; use int32, int64, float32 or bfloat16")
+    return names[t.dtype]
+
+
+def _check_tensors(name: str, ts, dtype: str, numel: int, device):
+    if not 1 <= len(ts) <= MAX_RANKS:
+        raise ValueError(f"{name}: between 1 and {MAX_RANKS} rank buffers, got {len(ts)}")
+    for r, t in enumerate(ts):
+        if not t.is_cuda:
+            raise ValueError(f"{name}[{r}] is not a CUDA tensor")
+        if t.device != device:
+            raise ValueError(f"{name}[{r}] is on {t.device}, expected {device}")
+        if _dtype_name(t) != dtype:
+            raise TypeError(f"{name}[{r}] has dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}[{r}] is not contiguous")
+        if t.numel() != numel:
+            raise ValueError(f"{name}[{r}] holds {t.numel()} elements, expected {numel}")
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptrs(ts):
+    return pointer_table([t.data_ptr() for t in ts])
+
+
+def vc_shard_count(count: int, nranks: int) -> int:
+    """q = ceil(count / nranks), the per-rank shard length."""
+    return int(lib().vc_shard_count(count, nranks))
+
+
+def vc_reduce_scatter(sendbufs, recvbufs, op: str = "sum", order: str = "ring", stream=None):
+    """recvbufs[r] (q elements) <- reduction of every sendbufs[s] (M elements)
+    over the indices of shard r; tail positions past M get the identity."""
+    n = len(sendbufs)
+    if len(recvbufs) != n:
+        raise ValueError("one output shard per rank")
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    q = vc_shard_count(M, n)
+    if any(t.numel() != q for t in recvbufs):
+        raise ValueError(
+            f"output shard must hold ceil(M/N) = {q} elements (M = {M}, N = {n}); "
+            f"input must be N times the (padded) output size")
+    _check_tensors("recvbufs", recvbufs, dt, q, dev)
+    check_status(lib().vc_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                         OPS[op], ORDERS[order], _stream(stream, dev)))
+
+
+def vc_all_gather(sendbufs, recvbufs, count: int | None = None, stream=None):
+    """recvbufs[r][s*q + j] <- sendbufs[s][j] for every r, trimmed to count
+    (default: recvbufs[0].numel())."""
+    n = len(sendbufs)
+    if len(recvbufs) != n:
+        raise ValueError("one output buffer per rank")
+    dt = _dtype_name(recvbufs[0])
+    M = recvbufs[0].numel() if count is None else int(count)
+    dev = recvbufs[0].device
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    q = vc_shard_count(M, n)
+    if any(t.numel() != q for t in sendbufs):
+        raise ValueError(f"input shard must hold ceil(M/N) = {q} elements (M = {M}, N = {n})")
+    _check_tensors("sendbufs", sendbufs, dt, q, dev)
+    check_status(lib().vc_all_gather(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                     _stream(stream, dev)))
+
+
+def vc_all_reduce(sendbufs, recvbufs=None, op: str = "sum", order: str = "ring", stream=None):
+    """recvbufs[r] <- elementwise reduction of all sendbufs, for every r.
+    recvbufs=None reduces in place."""
+    n = len(sendbufs)
+    recvbufs = list(sendbufs) if recvbufs is None else recvbufs
+    if len(recvbufs) != n:
+        raise ValueError("one output buffer per rank")
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    check_status(lib().vc_all_reduce(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                     OPS[op], ORDERS[order], _stream(stream, dev)))
+
+
+def vc_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum",
+                             order: str = "ring", stream=None):
+    """ReduceScatter into shardbufs (q elements each), then AllGather into
+    recvbufs (in place if None)."""
+    n = len(sendbufs)
+    recvbufs = list(sendbufs) if recvbufs is None else recvbufs
+    if len(recvbufs) != n or len(shardbufs) != n:
+        raise ValueError("one shard and one output buffer per rank")
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    q = vc_shard_count(M, n)
+    if any(t.numel() != q for t in shardbufs):
+        raise ValueError(f"shard buffers must hold ceil(M/N) = {q} elements")
+    _check_tensors("shardbufs", shardbufs, dt, q, dev)
+    check_status(lib().vc_all_reduce_decomposed(_ptrs(sendbufs), _ptrs(shardbufs),
+                                                _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
+                                                ORDERS[order], _stream(stream, dev)))

@@ -1,0 +1,301 @@
+// The C ABI of include/vc.h: argument checks on the host, then one launch
+// (two for the decomposed AllReduce) on the caller's stream.  Nothing is
+// allocated; the pointer tables travel by value in the kernel parameters.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "vc.h"
+#include "vc_device.cuh"
+
+namespace vc {
+
+namespace {
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlap(const Range& a, const Range& b) {
+    return a.lo < b.hi && b.lo < a.hi && a.lo < a.hi && b.lo < b.hi;
+}
+
+int elem_size(vc_dtype_t dt) {
+    switch (dt) {
+    case VC_INT32: return 4;
+    case VC_INT64: return 8;
+    case VC_FLOAT32: return 4;
+    case VC_BFLOAT16: return 2;
+    default: return 0;
+    }
+}
+
+bool valid_op(vc_op_t op) { return op >= VC_SUM && op <= VC_AVG; }
+bool valid_order(vc_order_t o) { return o >= VC_ORDER_RING && o <= VC_ORDER_PAIRWISE_TREE; }
+bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+// Common checks of every call.  *bytes_m and *bytes_q receive the byte sizes
+// of a full rank buffer (M elements) and of a shard (q elements).
+vc_status_t check_shape(int nranks, size_t count, vc_dtype_t dtype, size_t* bytes_m,
+                        size_t* bytes_q) {
+    if (nranks < 1 || nranks > VC_MAX_RANKS) return VC_ERR_INVALID_ARGUMENT;
+    const int es = elem_size(dtype);
+    if (es == 0) return VC_ERR_INVALID_ARGUMENT;
+    // element indices are signed 64-bit in the kernels; byte sizes must fit
+    if (count > (size_t)(1ULL << 62) / (size_t)es) return VC_ERR_INVALID_ARGUMENT;
+    const size_t q = vc_shard_count(count, nranks);
+    *bytes_m = count * (size_t)es;
+    *bytes_q = q * (size_t)es;
+    return VC_SUCCESS;
+}
+
+// Every buffer must be non-NULL and aligned to its element size (the
+// kernels' element-wise paths access whole elements).
+vc_status_t check_table(const void* const* t, int n, vc_dtype_t dtype) {
+    if (t == nullptr) return VC_ERR_INVALID_ARGUMENT;
+    const uintptr_t es = (uintptr_t)elem_size(dtype);
+    for (int r = 0; r < n; ++r)
+        if (t[r] == nullptr || reinterpret_cast<uintptr_t>(t[r]) % es != 0)
+            return VC_ERR_INVALID_ARGUMENT;
+    return VC_SUCCESS;
+}
+
+Range range_of(const void* p, size_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+
+// Outputs must be pairwise disjoint and disjoint from every input, except
+// that output r may be exactly input r when allow_in_place is set.
+vc_status_t check_alias(const void* const* in, size_t in_bytes, void* const* out,
+                        size_t out_bytes, int n, bool allow_in_place) {
+    for (int r = 0; r < n; ++r) {
+        const Range o = range_of(out[r], out_bytes);
+        for (int s = 0; s < n; ++s) {
+            if (s != r && overlap(o, range_of(out[s], out_bytes))) return VC_ERR_ALIAS;
+            const Range i = range_of(in[s], in_bytes);
+            if (!overlap(o, i)) continue;
+            const bool same = allow_in_place && s == r && in[s] == out[r] && in_bytes == out_bytes;
+            if (!same) return VC_ERR_ALIAS;
+        }
+    }
+    return VC_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Test hook: with VC_TEST_FAIL_LAUNCH set to a non-zero value the next
+// launches report a launch failure instead of launching.  Lets the error path
+// be exercised without a faulty kernel.
+bool injected_launch_failure() {
+    const char* v = getenv("VC_TEST_FAIL_LAUNCH");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+vc_status_t launch_reduce(const void* const* in, void* const* out, int n, size_t count,
+                          vc_dtype_t dtype, vc_op_t op, vc_order_t order, bool rs,
+                          cudaStream_t st) {
+    ReduceParams p;
+    memset(&p, 0, sizeof p);
+    const long long M = (long long)count;
+    const long long q = (long long)vc_shard_count(count, n);
+    bool vec = true;
+    for (int r = 0; r < n; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = out[r];
+        vec = vec && aligned16(in[r]) && (rs || aligned16(out[r]));
+    }
+    p.M = M;
+    p.q = q;
+    p.limit = rs ? (long long)n * q : M;
+    p.inv_q = 1.0f / (float)q;
+    p.n = n;
+    p.avg = (op == VC_AVG);
+    p.vec_ok = vec;
+    if (injected_launch_failure()) return VC_ERR_CUDA;
+    cudaError_t e;
+    switch (dtype) {
+    case VC_INT32: e = launch_reduce_i32(p, (int)op, (int)order, rs, st); break;
+    case VC_INT64: e = launch_reduce_i64(p, (int)op, (int)order, rs, st); break;
+    case VC_FLOAT32: e = launch_reduce_f32(p, (int)op, (int)order, rs, st); break;
+    case VC_BFLOAT16: e = launch_reduce_bf16(p, (int)op, (int)order, rs, st); break;
+    default: return VC_ERR_INVALID_ARGUMENT;
+    }
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+}
+
+vc_status_t launch_all_gather(const void* const* in, void* const* out, int n, size_t count,
+                              vc_dtype_t dtype, cudaStream_t st) {
+    GatherParams p;
+    memset(&p, 0, sizeof p);
+    bool vec = true;
+    for (int r = 0; r < n; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = out[r];
+        vec = vec && aligned16(out[r]);
+    }
+    p.M = (long long)count;
+    p.q = (long long)vc_shard_count(count, n);
+    p.inv_q = 1.0f / (float)p.q;
+    p.n = n;
+    p.vec_ok = vec;
+    if (injected_launch_failure()) return VC_ERR_CUDA;
+    const cudaError_t e = launch_gather(p, elem_size(dtype), st);
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+}
+
+}  // namespace
+
+// Grid size for the grid-stride kernels: one block per 256 vectors, capped
+// at the blocks that fit on all SMs at once (queried once per kernel).
+int grid_blocks(const void* kernel, long long nvec) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> per_sm;
+    static int sm_count[VC_MAX_RANKS] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= VC_MAX_RANKS) return -1;
+    int occ = 0, sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (sm_count[dev] == 0) {
+            int v = 0;
+            if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return -1;
+            sm_count[dev] = v;
+        }
+        sms = sm_count[dev];
+        auto it = per_sm.find(kernel);
+        if (it == per_sm.end()) {
+            int v = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kThreads, 0) !=
+                cudaSuccess)
+                return -1;
+            it = per_sm.emplace(kernel, v < 1 ? 1 : v).first;
+        }
+        occ = it->second;
+    }
+    const long long want = (nvec + kThreads - 1) / kThreads;
+    const long long cap = (long long)sms * occ;
+    long long b = want < cap ? want : cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st) {
+    const long long nvec = (p.M * esize + 15) / 16;
+    int blocks;
+    switch (esize) {
+    case 2:
+        blocks = grid_blocks((const void*)vc_ag_kernel<2>, nvec);
+        if (blocks < 1) return cudaErrorInvalidConfiguration;
+        vc_ag_kernel<2><<<blocks, kThreads, 0, st>>>(p);
+        break;
+    case 4:
+        blocks = grid_blocks((const void*)vc_ag_kernel<4>, nvec);
+        if (blocks < 1) return cudaErrorInvalidConfiguration;
+        vc_ag_kernel<4><<<blocks, kThreads, 0, st>>>(p);
+        break;
+    case 8:
+        blocks = grid_blocks((const void*)vc_ag_kernel<8>, nvec);
+        if (blocks < 1) return cudaErrorInvalidConfiguration;
+        vc_ag_kernel<8><<<blocks, kThreads, 0, st>>>(p);
+        break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace vc
+
+using namespace vc;
+
+extern "C" {
+
+size_t vc_shard_count(size_t count, int nranks) {
+    if (nranks < 1) return 0;
+    return count / (size_t)nranks + (count % (size_t)nranks != 0 ? 1 : 0);
+}
+
+vc_status_t vc_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                              size_t count, vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                              vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
+    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (count == 0) return VC_SUCCESS;
+    if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_alias(sendbufs, bm, recvbufs, bq, nranks, false)) != VC_SUCCESS) return s;
+    return launch_reduce(sendbufs, recvbufs, nranks, count, dtype, op, order, true,
+                         static_cast<cudaStream_t>(stream));
+}
+
+vc_status_t vc_all_gather(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                          size_t count, vc_dtype_t dtype, vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (count == 0) return VC_SUCCESS;
+    if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_alias(sendbufs, bq, recvbufs, bm, nranks, false)) != VC_SUCCESS) return s;
+    return launch_all_gather(sendbufs, recvbufs, nranks, count, dtype,
+                             static_cast<cudaStream_t>(stream));
+}
+
+vc_status_t vc_all_reduce(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                          size_t count, vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                          vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
+    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (count == 0) return VC_SUCCESS;
+    if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_alias(sendbufs, bm, recvbufs, bm, nranks, true)) != VC_SUCCESS) return s;
+    return launch_reduce(sendbufs, recvbufs, nranks, count, dtype, op, order, false,
+                         static_cast<cudaStream_t>(stream));
+}
+
+vc_status_t vc_all_reduce_decomposed(const void* const* sendbufs, void* const* shardbufs,
+                                     void* const* recvbufs, int nranks, size_t count,
+                                     vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                                     vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
+    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (count == 0) return VC_SUCCESS;
+    if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(shardbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    // shards overlap neither the inputs nor the outputs nor each other
+    if ((s = check_alias(sendbufs, bm, shardbufs, bq, nranks, false)) != VC_SUCCESS) return s;
+    if ((s = check_alias(const_cast<const void* const*>(recvbufs), bm, shardbufs, bq, nranks,
+                         false)) != VC_SUCCESS)
+        return s;
+    if ((s = check_alias(sendbufs, bm, recvbufs, bm, nranks, true)) != VC_SUCCESS) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = launch_reduce(sendbufs, shardbufs, nranks, count, dtype, op, order, true, st);
+    if (s != VC_SUCCESS) return s;
+    return launch_all_gather(const_cast<const void* const*>(shardbufs), recvbufs, nranks, count,
+                             dtype, st);
+}
+
+const char* vc_status_string(vc_status_t status) {
+    switch (status) {
+    case VC_SUCCESS: return "success";
+    case VC_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case VC_ERR_UNSUPPORTED: return "unsupported: this order needs a power-of-two rank count";
+    case VC_ERR_ALIAS: return "an output buffer overlaps an input or another output";
+    case VC_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

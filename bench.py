@@ -1,0 +1,530 @@
+"""Bench of the virtual-rank collectives: HBM GB/s and fraction of the
+measured copy peak.
+
+One step = the whole path once over the workload: the fused AllReduce
+(vc_all_reduce, one kernel) and the decomposed AllReduce
+(vc_all_reduce_decomposed: ReduceScatter kernel, then AllGather kernel).
+Default workload: four virtual ranks of 256 MiB fp32 (67,108,864 elements,
+normal(0, 1)), SUM, ring order.
+
+Algorithmic bytes (s = element size, q = ceil(M/N)):
+  ReduceScatter  N*M*s read + M*s written
+  AllGather      M*s read   + N*M*s written
+  fused AR       N*M*s read + N*M*s written
+  decomposed AR  RS + AG
+The step moves 4*N*M*s + 2*M*s bytes; value = those bytes / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(the path shards by index range with no exchange; weak scaling), the step
+time is the max over ranks, and value counts the bytes of all ranks.
+--impl reference times the CPU oracle instead, on a bounded window of the
+same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "AR/RS/AG HBM GB/s over N virtual ranks; % of GB300 HBM copy peak"
+FALLBACK_HBM_GBS = 6800.0
+ESIZE = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}
+DTYPE_TAG = {"int32": "i32", "int64": "i64", "float32": "f32", "bfloat16": "bf16"}
+
+
+# ----------------------------------------------------------------- helpers --
+
+def step_bytes(n: int, M: int, es: int) -> dict:
+    rs = n * M * es + M * es
+    ag = M * es + n * M * es
+    ar = 2 * n * M * es
+    return {"reduce_scatter": rs, "all_gather": ag, "fused_ar": ar, "decomposed_ar": rs + ag,
+            "step": ar + rs + ag}
+
+
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "allreduce_reducescatter_allgather_gb300" / "csrc").glob("*")):
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = ROOT / "profiles" / "dram_traffic.txt"
+    if not p.exists():
+        return None
+    rec = {}
+    for line in p.read_text().splitlines():
+        if line.startswith("#") or ":" not in line:
+            continue
+        k, _, v = line.partition(":")
+        rec[k.strip()] = v.strip()
+    key = f"{kernel}@{workload}"
+    if rec.get("source_sha") != source_digest() or key not in rec:
+        return None
+    return float(rec[key])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index  # nvidia-smi --id: an index or a GPU UUID
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "") else 0.0,
+                             "hw_slowdown": parts[6], "hw_thermal": parts[7],
+                             "sw_thermal": parts[8], "sw_power_cap": parts[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] >= 0.5 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in loaded:
+            for k in ("hw_slowdown", "hw_thermal", "sw_thermal", "sw_power_cap"):
+                if r[k] == "Active":
+                    reasons.add(k if k != "hw_thermal" else "hw_thermal_slowdown")
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "samples": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(torch, local_ms: float, local_bytes: int, world: int):
+    """Max step time and total bytes over ranks (control plane only)."""
+    if world == 1:
+        return local_ms, local_bytes
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() \
+        else torch.device("cpu")
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_window_step(xs, dtype, op, order):
+    """One oracle step over host windows: fused AR then decomposed AR."""
+    import oracle
+    oracle.all_reduce(xs, dtype, op, order)
+    oracle.all_reduce_decomposed(xs, dtype, op, order)
+
+
+def host_window(workload: dict, window: int):
+    import synthetic_inputs as si
+    w = dict(workload)
+    n, M = w.pop("n"), w.pop("M")
+    dtype, dist_, seed = w.pop("dtype"), w.pop("dist"), w.pop("seed")
+    return si.generate(dtype, dist_, n, min(window, M), seed=seed, **w)
+
+
+def time_oracle(workload: dict, op: str, order: str, seconds: float, window: int):
+    """Run oracle steps over a window of `window` elements per rank until
+    `seconds` of CPU time have passed; returns (GB/s, steps, seconds)."""
+    xs = host_window(workload, window)
+    n, dtype = workload["n"], workload["dtype"]
+    W = xs[0].size
+    b = step_bytes(n, W, ESIZE[dtype])["step"]
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_window_step(xs, dtype, op, order)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return b * steps / el / 1e9, steps, el
+
+
+def run_reference(args, workload: dict):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    n, dtype = workload["n"], workload["dtype"]
+    # size the window so that warmup + steps take about a minute
+    calib = host_window(workload, 1 << 16)
+    t0 = time.perf_counter()
+    oracle_window_step(calib, dtype, args.op, args.order)
+    per_elem = (time.perf_counter() - t0) / calib[0].size
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    window = 1 << 12
+    while window * 2 * per_elem <= budget and window * 2 <= workload["M"]:
+        window *= 2
+    xs = host_window(workload, window)
+    W = xs[0].size
+    for _ in range(args.warmup):
+        oracle_window_step(xs, dtype, args.op, args.order)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_window_step(xs, dtype, args.op, args.order)
+    el = time.perf_counter() - t0
+    b = step_bytes(n, W, ESIZE[dtype])["step"]
+    value = b * args.steps / el / 1e9
+    sample = (f"the first {W} of {workload['M']} elements of each of the {n} ranks; "
+              f"each step = oracle fused AR + decomposed AR on that window")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TAG[dtype], "data": "synthetic",
+        "config": config_block(args, workload, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(args, workload, world):
+    n, M, dtype = workload["n"], workload["M"], workload["dtype"]
+    return {
+        "workload": args.workload,
+        "virtual_ranks": n, "elements_per_rank": M, "bytes_per_rank": M * ESIZE[dtype],
+        "op": args.op, "order": args.order,
+        "step": "fused AllReduce + decomposed AllReduce (ReduceScatter then AllGather)",
+        "l2": "no flush: every step streams 2 GiB of inputs and outputs per call, "
+              "far larger than the 129 MB L2",
+        "parallelism": f"{world} GPU(s), each with its own {n} virtual ranks (index-range "
+                       "shards, no exchange)",
+    }
+
+
+# ------------------------------------------------------------ GPU arm ----
+
+def run_ours(args, workload: dict):
+    import torch
+
+    import allreduce_reducescatter_allgather_gb300 as vc
+    import synthetic_inputs as si
+
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = dict(workload)
+    n, M, dtype = w.pop("n"), w.pop("M"), w.pop("dtype")
+    d = si.generate_device(torch, dtype, w.pop("dist"), n, M, w.pop("seed") + rank, dev, **w)
+    q = vc.vc_shard_count(M, n)
+    es = ESIZE[dtype]
+    y = [torch.empty_like(t) for t in d]
+    y2 = [torch.empty_like(t) for t in d]
+    sh = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+    by = step_bytes(n, M, es)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vc.vc_all_reduce(d, y, op=args.op, order=args.order, stream=stream)
+        vc.vc_all_reduce_decomposed(d, sh, y2, op=args.op, order=args.order, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        gpu_id = local
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    # per-call events on the launching stream: [AR start, AR end = dec start, dec end]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        e = evs[k]
+        e[0].record(stream)
+        vc.vc_all_reduce(d, y, op=args.op, order=args.order, stream=stream)
+        e[1].record(stream)
+        vc.vc_all_reduce_decomposed(d, sh, y2, op=args.op, order=args.order, stream=stream)
+        e[2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    ar_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    max_ms, all_bytes = aggregate(torch, total_ms, by["step"] * args.steps, world)
+    ms_per_step = max_ms / args.steps
+    value = all_bytes / (max_ms / 1e3) / 1e9
+
+    # RS alone and AG alone (outside the timed region), for the per-path table
+    def time_calls(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(10, min(200, args.steps))
+    rs_ms = time_calls(lambda: vc.vc_reduce_scatter(d, sh, op=args.op, order=args.order,
+                                                    stream=stream), reps)
+    ag_ms = time_calls(lambda: vc.vc_all_gather(sh, y2, stream=stream), reps)
+
+    peak, peak_kind = measured_peak()
+    ar_avg = statistics.mean(ar_ms)
+    dec_avg = statistics.mean(dec_ms)
+
+    def path(bytes_, ms):
+        g = bytes_ / (ms / 1e3) / 1e9
+        return {"us": round(ms * 1e3, 2), "gbs": round(g, 1), "frac": round(g / peak, 4)}
+
+    paths = {"fused_ar": path(by["fused_ar"], ar_avg),
+             "decomposed_ar": path(by["decomposed_ar"], dec_avg),
+             "reduce_scatter": path(by["reduce_scatter"], rs_ms),
+             "all_gather": path(by["all_gather"], ag_ms)}
+    ar_gbs = by["fused_ar"] / (ar_avg / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "vc_ar_kernel", "achieved": round(ar_gbs, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(ar_gbs / peak, 4),
+                "traffic": recorded_traffic("vc_ar_kernel", args.workload),
+                "algorithmic_bytes_per_launch": by["fused_ar"]}
+
+    memory = memory_report(torch, vc, d, args, dev) if not args.no_memory else None
+    e2e = e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, by["step"])
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_TAG[dtype], "data": "synthetic",
+        "config": config_block(args, workload, world),
+        "roofline": roofline,
+        "paths": paths,
+        "gpu_launches": 3 * args.steps,
+        "e2e": e2e,
+    }
+    if clk is not None:
+        line["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                          "reasons": clk["reasons"], "samples": clk["samples"]}
+    if memory is not None:
+        line["memory_mib"] = memory
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        g, steps, secs = time_oracle(workload, args.op, args.order, args.cpu_seconds,
+                                     window=1 << 22)
+        line["cpu_baseline"] = {
+            "value": round(g, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} oracle steps (fused AR + decomposed AR) over the first "
+                      f"{min(1 << 22, M)} elements of each of the {n} ranks, "
+                      f"{secs:.1f} s on one host core"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, step_bytes_):
+    """The same step through the public API with the inputs in pinned host
+    memory: each step copies the inputs in, runs both AllReduce paths and
+    copies every output back."""
+    n = len(d)
+    host_in = [t.cpu().pin_memory() for t in d]
+    host_y = [torch.empty_like(t, device="cpu").pin_memory() for t in d]
+    host_y2 = [torch.empty_like(t, device="cpu").pin_memory() for t in d]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = 2 * h2d
+
+    def one():
+        for r in range(n):
+            d[r].copy_(host_in[r], non_blocking=True)
+        vc.vc_all_reduce(d, y, op=args.op, order=args.order, stream=stream)
+        vc.vc_all_reduce_decomposed(d, sh, y2, op=args.op, order=args.order, stream=stream)
+        for r in range(n):
+            host_y[r].copy_(y[r], non_blocking=True)
+            host_y2[r].copy_(y2[r], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.e2e_steps
+    return {"value": round(step_bytes_ / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": args.e2e_steps}
+
+
+def memory_report(torch, vc, d, args, dev):
+    """Peak device memory (MiB above the baseline) of the buffer lifetimes of
+    "NCCL 专家课程 07" 显存实验, with all N virtual ranks on one GPU: inputs
+    are copies of the workload made inside each measurement."""
+    n, M = len(d), d[0].numel()
+    q = vc.vc_shard_count(M, n)
+    MiB = float(1 << 20)
+    out = {}
+
+    def measure(name, fn):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        kept = fn()
+        torch.cuda.synchronize()
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        steady = torch.cuda.memory_allocated(dev) - base
+        out[name] = {"peak": round(peak / MiB, 1), "steady": round(steady / MiB, 1)}
+        del kept
+
+    def ar_in_place():
+        full = [t.clone() for t in d]
+        vc.vc_all_reduce(full, None, op=args.op, order=args.order)
+        return full
+
+    def ar_out_of_place():
+        full = [t.clone() for t in d]
+        res = [torch.empty_like(t) for t in full]
+        vc.vc_all_reduce(full, res, op=args.op, order=args.order)
+        del full
+        return res
+
+    def rs_only():
+        full = [t.clone() for t in d]
+        shard = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+        vc.vc_reduce_scatter(full, shard, op=args.op, order=args.order)
+        torch.cuda.synchronize()
+        del full
+        return shard
+
+    def rs_ag_naive():
+        full = [t.clone() for t in d]
+        shard = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+        gathered = [torch.empty_like(t) for t in full]
+        vc.vc_reduce_scatter(full, shard, op=args.op, order=args.order)
+        vc.vc_all_gather(shard, gathered)
+        torch.cuda.synchronize()
+        del full, shard
+        return gathered
+
+    def rs_ag_optimized():
+        full = [t.clone() for t in d]
+        shard = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+        vc.vc_reduce_scatter(full, shard, op=args.op, order=args.order)
+        torch.cuda.synchronize()
+        del full
+        gathered = [torch.empty(M, dtype=d[0].dtype, device=dev) for _ in range(n)]
+        vc.vc_all_gather(shard, gathered)
+        torch.cuda.synchronize()
+        del shard
+        return gathered
+
+    for name, fn in (("allreduce_in_place", ar_in_place),
+                     ("allreduce_out_of_place", ar_out_of_place),
+                     ("reduce_scatter_only", rs_only), ("rs_ag_naive", rs_ag_naive),
+                     ("rs_ag_optimized", rs_ag_optimized)):
+        measure(name, fn)
+    return out
+
+
+def main(argv=None):
+    import synthetic_inputs as si
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="n4_256mib_f32_normal", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--op", default="sum", choices=["sum", "prod", "max", "min", "avg"])
+    ap.add_argument("--order", default="ring",
+                    choices=["ring", "recursive_halving", "pairwise_tree"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-memory", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    workload = si.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, workload)
+    if dist_info()[0] == 1:
+        import __graft_entry__
+        __graft_entry__.build()  # under torchrun the library must be built beforehand
+    return run_ours(args, workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

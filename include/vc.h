@@ -1,0 +1,177 @@
+/*
+ * vc.h -- AllReduce, ReduceScatter and AllGather over N virtual ranks held
+ * in one GPU's memory.
+ *
+ * A "virtual rank" is one device buffer.  Every call takes host arrays of N
+ * device pointers (one per rank), the logical per-rank element count M, the
+ * element type, the reduction op and the reduction order, and enqueues one
+ * kernel (two for the decomposed AllReduce) on the caller's CUDA stream.
+ *
+ * Definitions ("NCCL 专家课程 07：AllReduce 等价分解、显存生命周期与 Kernel
+ * 证据", section 数学证明; q = ceil(M/N)):
+ *   AllReduce      y^(r)_i        = (+)_{s=0}^{N-1} x^(s)_i,   0 <= i < M, every r
+ *   ReduceScatter  z^(r)_j        = (+)_{s=0}^{N-1} x^(s)_{rq+j}, 0 <= j < q
+ *   AllGather      yhat^(r)_{sq+j} = z^(s)_j   (source-rank-major), trimmed to M
+ * with the inputs padded from M to Nq with the op's identity (same page,
+ * 条件三: 0 for sum, 1 for prod, the type's minimum / -inf for max, the
+ * maximum / +inf for min; never 0 for max).  The padding is virtual: indices
+ * >= M are read as the identity and never stored anywhere.
+ *
+ * Counts follow NCCL's rule that the ReduceScatter output count is the
+ * AllGather input count (same page, 源码一): every call takes the logical M;
+ * ReduceScatter writes q elements per rank and AllGather reads q per rank.
+ *
+ * Ownership and lifetime: the caller owns every buffer; the library never
+ * allocates device memory and keeps no pointer after a call returns (the
+ * pointer tables are copied by value into the kernel's parameters).  Calls
+ * are asynchronous on `stream`; results are valid once the stream has
+ * passed the call.  Every buffer must be aligned to its element size; when
+ * every base pointer involved is also 16-byte aligned the kernels use
+ * 16-byte vector accesses for the bulk of the data (otherwise they fall back
+ * to element-wise accesses, on the GPU).
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; on
+ * any error the call returns a non-zero status and launches nothing (the
+ * pages' capacity check also rejects before any kernel, 源码五 and Contract
+ * 实验四).  VC_ERR_CUDA reports a failed launch; nothing else is retried.
+ * All entry points are thread-safe; calls enqueued on different streams
+ * that write overlapping memory race, as any two kernels would.
+ */
+#ifndef VC_H
+#define VC_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The largest number of virtual ranks one call takes. */
+#define VC_MAX_RANKS 64
+
+/* Element types.  Integers accumulate in 64 bits and wrap modulo 2^64
+ * (int32 results are the low 32 bits); float32 accumulates in float32;
+ * bfloat16 is widened exactly to float32, accumulated in float32 and rounded
+ * once to nearest-even at the store.  (The pages fix no accumulator for
+ * bf16; they note that float reduction is not associative, 条件五.) */
+typedef enum {
+    VC_INT32 = 0,
+    VC_INT64 = 1,
+    VC_FLOAT32 = 2,
+    VC_BFLOAT16 = 3
+} vc_dtype_t;
+
+/* Reduction ops ("通信与互联（01）：集合通信原语与代价模型", 二.1: sum, max,
+ * min, prod, avg).  AVG is the SUM in the chosen order divided once by N:
+ * one IEEE single division for float types, truncation toward zero for
+ * integers.  MAX/MIN keep the running value on ties.  NaN inputs are outside
+ * the contract. */
+typedef enum {
+    VC_SUM = 0,
+    VC_PROD = 1,
+    VC_MAX = 2,
+    VC_MIN = 3,
+    VC_AVG = 4
+} vc_op_t;
+
+/* Reduction orders.  For integers and for MAX/MIN every order gives the same
+ * bits; for float SUM/PROD/AVG the order is part of the result (条件五).
+ * Element i lies in chunk c = floor(i/q).
+ *  RING: the ring ReduceScatter schedule ("Ring AllReduce 核心流程" and
+ *    "通信与互联（01）" 五.2: at step s rank r sends chunk (r-s+1) mod N and
+ *    adds the chunk it receives into its own copy; rank r ends owning chunk
+ *    (r+1) mod N).  Chunk c's value is
+ *    (((x^(c) (+) x^(c+1)) (+) x^(c+2)) ... (+) x^(c+N-1)), ranks mod N.
+ *    Any N from 1 to VC_MAX_RANKS.
+ *  RECURSIVE_HALVING: step j pairs ranks at distance N/2^j and each keeps
+ *    the combination of its half with its partner's ("ReduceScatter" page,
+ *    Recursive Halving; N=8 pairs (0,4)(1,5)(2,6)(3,7), (0,2)..., (0,1)...).
+ *    The value is the balanced pairwise tree over the ranks in bit-reversed
+ *    order, e.g. ((x0(+)x4)(+)(x2(+)x6))(+)((x1(+)x5)(+)(x3(+)x7)).  N must be
+ *    a power of two (the page's hypercube condition).
+ *  PAIRWISE_TREE: the binary tree of "通信与互联（01）" 六.1 (rank 0 the root
+ *    with the single child N/2; rank r's level is its lowest set bit L and its
+ *    parent is (r-L) | 2L; odd ranks are leaves).  An inner node's value is
+ *    (left subtree (+) right subtree) (+) its own operand, the lower-ranked
+ *    child on the left.  N must be a power of two. */
+typedef enum {
+    VC_ORDER_RING = 0,
+    VC_ORDER_RECURSIVE_HALVING = 1,
+    VC_ORDER_PAIRWISE_TREE = 2
+} vc_order_t;
+
+typedef enum {
+    VC_SUCCESS = 0,
+    /* a NULL pointer table or buffer, a buffer not aligned to its element
+     * size, nranks outside [1, VC_MAX_RANKS], an unknown enum value, or a
+     * count whose byte size exceeds 2^62 */
+    VC_ERR_INVALID_ARGUMENT = 1,
+    /* RECURSIVE_HALVING or PAIRWISE_TREE with nranks not a power of two */
+    VC_ERR_UNSUPPORTED = 2,
+    /* an output range overlaps an input range or another output range (the
+     * only overlap allowed is the in-place AllReduce, recvbufs[r] ==
+     * sendbufs[r] exactly) */
+    VC_ERR_ALIAS = 3,
+    /* the CUDA runtime refused the launch or a device query.  (Setting the
+     * environment variable VC_TEST_FAIL_LAUNCH to a non-zero value makes
+     * every call that passes its checks return this without launching: a
+     * test hook for the error path.) */
+    VC_ERR_CUDA = 4
+} vc_status_t;
+
+/* A cudaStream_t, passed as an opaque pointer; NULL is the legacy default
+ * stream. */
+typedef void *vc_stream_t;
+
+/* q = ceil(count / nranks): the shard length ReduceScatter writes and
+ * AllGather reads per rank.  Returns 0 when nranks < 1. */
+size_t vc_shard_count(size_t count, int nranks);
+
+/* ReduceScatter.  sendbufs[s] (s < nranks): device buffer of `count`
+ * elements, rank s's input x^(s).  recvbufs[r]: device buffer of
+ * q = vc_shard_count(count, nranks) elements, receives z^(r); positions j with
+ * r*q + j >= count receive the op's identity (0 for AVG).  No recv buffer may
+ * overlap any send buffer or another recv buffer.  count == 0 returns
+ * VC_SUCCESS without launching. */
+vc_status_t vc_reduce_scatter(const void *const *sendbufs, void *const *recvbufs, int nranks,
+                              size_t count, vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                              vc_stream_t stream);
+
+/* AllGather.  sendbufs[s]: device buffer of q = vc_shard_count(count,
+ * nranks) elements, shard s.  recvbufs[r]: device buffer of `count`
+ * elements; receives shard s at offset s*q for every s, trimmed to `count`
+ * (elements of the last shard past `count` are not read).  No recv buffer
+ * may overlap a send buffer or another recv buffer.  AllGather moves bits
+ * only; it takes no op or order. */
+vc_status_t vc_all_gather(const void *const *sendbufs, void *const *recvbufs, int nranks,
+                          size_t count, vc_dtype_t dtype, vc_stream_t stream);
+
+/* AllReduce in one kernel: every element is read once from each of the N
+ * inputs, reduced in registers and written to all N outputs (the single-GPU
+ * counterpart of a ring AllReduce that fuses its last reduction with the
+ * first forward of the gather phase, "NCCL 专家课程 07" 源码三).
+ * sendbufs[s], recvbufs[r]: device buffers of `count` elements.  In place is
+ * allowed per rank (recvbufs[r] == sendbufs[r]); any other overlap is
+ * VC_ERR_ALIAS. */
+vc_status_t vc_all_reduce(const void *const *sendbufs, void *const *recvbufs, int nranks,
+                          size_t count, vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                          vc_stream_t stream);
+
+/* AllReduce as two kernels: ReduceScatter into shardbufs (N buffers of q
+ * elements, scratch owned by the caller), then AllGather from them into
+ * recvbufs ("NCCL 专家课程 07", 源码四/五: two separate collectives).  Gives
+ * the same bits as vc_all_reduce in the same order.  recvbufs[r] ==
+ * sendbufs[r] is allowed; shard buffers may overlap nothing. */
+vc_status_t vc_all_reduce_decomposed(const void *const *sendbufs, void *const *shardbufs,
+                                     void *const *recvbufs, int nranks, size_t count,
+                                     vc_dtype_t dtype, vc_op_t op, vc_order_t order,
+                                     vc_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *vc_status_string(vc_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VC_H */

@@ -1,0 +1,236 @@
+"""The C ABI without a GPU: the library loads, exports what the header
+declares, and rejects bad arguments before launching anything.
+
+No call here reaches a kernel launch: either validation fails first, or the
+launch hook (VC_TEST_FAIL_LAUNCH) turns the launch into VC_ERR_CUDA.  The
+fake device pointers below are never dereferenced.
+"""
+from __future__ import annotations
+
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+SUCCESS, INVALID, UNSUPPORTED, ALIAS, CUDA = 0, 1, 2, 3, 4
+I32, I64, F32, BF16 = 0, 1, 2, 3
+SUM, PROD, MAX, MIN, AVG = 0, 1, 2, 3, 4
+RING, RH, TREE = 0, 1, 2
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def vc():
+    import __graft_entry__
+    __graft_entry__.build()
+    import allreduce_reducescatter_allgather_gb300 as pkg
+    return pkg
+
+
+@pytest.fixture(autouse=True)
+def no_launch(monkeypatch):
+    # any call that passes validation reports a launch failure instead of
+    # launching: the pointers here are not real device memory
+    monkeypatch.setenv("VC_TEST_FAIL_LAUNCH", "1")
+
+
+def fake(n, base, stride=16 * MiB):
+    return [base + r * stride for r in range(n)]
+
+
+def table(vc, ptrs):
+    from allreduce_reducescatter_allgather_gb300._binding import pointer_table
+    return pointer_table(ptrs)
+
+
+def header_functions():
+    text = (ROOT / "include" / "vc.h").read_text()
+    return sorted(set(re.findall(r"^\S.*?\b(vc_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    assert names == sorted(["vc_shard_count", "vc_reduce_scatter", "vc_all_gather",
+                            "vc_all_reduce", "vc_all_reduce_decomposed", "vc_status_string"])
+
+
+def test_library_exports_every_declared_symbol(vc):
+    from allreduce_reducescatter_allgather_gb300._binding import EXPORTS, LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", str(LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (vc_\w+)$", out, flags=re.M))
+    for name in header_functions():
+        assert name in exported, name
+        assert hasattr(vc.lib(), name)
+    assert set(EXPORTS) == set(header_functions())
+
+
+def test_shard_count(vc):
+    L = vc.lib()
+    assert L.vc_shard_count(20, 4) == 5
+    assert L.vc_shard_count(1003, 4) == 251
+    assert L.vc_shard_count(1_000_003, 8) == 125_001
+    assert L.vc_shard_count(0, 4) == 0
+    assert L.vc_shard_count(3, 8) == 1
+    assert L.vc_shard_count(10, 0) == 0
+
+
+def test_status_strings(vc):
+    L = vc.lib()
+    for code in range(5):
+        assert L.vc_status_string(code)
+    assert b"unknown" in L.vc_status_string(99)
+
+
+def rs(vc, send, recv, n, M, dt=F32, op=SUM, order=RING):
+    return vc.lib().vc_reduce_scatter(table(vc, send) if send is not None else None,
+                                      table(vc, recv) if recv is not None else None,
+                                      n, M, dt, op, order, None)
+
+
+def ar(vc, send, recv, n, M, dt=F32, op=SUM, order=RING):
+    return vc.lib().vc_all_reduce(table(vc, send), table(vc, recv), n, M, dt, op, order, None)
+
+
+def ag(vc, send, recv, n, M, dt=F32):
+    return vc.lib().vc_all_gather(table(vc, send), table(vc, recv), n, M, dt, None)
+
+
+def dec(vc, send, shard, recv, n, M, dt=F32, op=SUM, order=RING):
+    return vc.lib().vc_all_reduce_decomposed(table(vc, send), table(vc, shard), table(vc, recv),
+                                             n, M, dt, op, order, None)
+
+
+def test_rank_count_limits(vc):
+    for n in (0, -1, 65):
+        k = max(n, 1)
+        assert rs(vc, fake(k, 1 << 40), fake(k, 2 << 40), n, 1000) == INVALID
+        assert ar(vc, fake(k, 1 << 40), fake(k, 2 << 40), n, 1000) == INVALID
+    assert ar(vc, fake(64, 1 << 40), fake(64, 2 << 40), 64, 1000) == CUDA  # valid: hook fires
+
+
+def test_unknown_enums(vc):
+    s, r = fake(4, 1 << 40), fake(4, 2 << 40)
+    assert rs(vc, s, r, 4, 100, dt=9) == INVALID
+    assert rs(vc, s, r, 4, 100, op=5) == INVALID
+    assert rs(vc, s, r, 4, 100, order=3) == INVALID
+    assert ar(vc, s, r, 4, 100, dt=-1) == INVALID
+    assert ag(vc, s, r, 4, 100, dt=7) == INVALID
+
+
+def test_null_pointers(vc):
+    assert rs(vc, None, fake(4, 2 << 40), 4, 100) == INVALID
+    assert rs(vc, fake(4, 1 << 40), None, 4, 100) == INVALID
+    s = fake(4, 1 << 40)
+    s[2] = 0
+    assert ar(vc, s, fake(4, 2 << 40), 4, 100) == INVALID
+    assert ag(vc, fake(4, 1 << 40), s, 4, 100) == INVALID
+
+
+def test_count_zero_launches_nothing(vc):
+    # succeeds without launching (the launch hook would report CUDA otherwise)
+    assert rs(vc, None, None, 4, 0) == SUCCESS
+    assert ar(vc, fake(4, 1 << 40), fake(4, 2 << 40), 4, 0) == SUCCESS
+    assert ag(vc, fake(4, 1 << 40), fake(4, 2 << 40), 4, 0) == SUCCESS
+
+
+def test_power_of_two_orders(vc):
+    """Recursive halving needs N = 2^k (the hypercube condition on the
+    "ReduceScatter" page); the tree order is read the same way."""
+    for n in (3, 5, 6, 12, 63):
+        s, r = fake(n, 1 << 40), fake(n, 2 << 40)
+        assert rs(vc, s, r, n, 1000, order=RH) == UNSUPPORTED
+        assert ar(vc, s, r, n, 1000, order=TREE) == UNSUPPORTED
+        assert ar(vc, s, r, n, 1000, order=RING) == CUDA
+    for n in (1, 2, 4, 8, 16, 32, 64):
+        s, r = fake(n, 1 << 40), fake(n, 2 << 40)
+        assert ar(vc, s, r, n, 1000, order=RH) == CUDA
+        assert rs(vc, s, r, n, 1000, order=TREE) == CUDA
+
+
+def test_alias_rules(vc):
+    n, M = 4, 1000
+    bytes_m = M * 4
+    s = fake(n, 1 << 40)
+    # in-place AllReduce per rank is allowed
+    assert ar(vc, s, list(s), n, M) == CUDA
+    # an output that is another rank's input is not
+    r = list(s)
+    r[0], r[1] = s[1], s[0]
+    assert ar(vc, s, r, n, M) == ALIAS
+    # partial overlap with its own input is not
+    r = list(s)
+    r[2] = s[2] + 4
+    assert ar(vc, s, r, n, M) == ALIAS
+    # two outputs overlapping each other
+    r = fake(n, 2 << 40)
+    r[3] = r[2] + bytes_m - 4
+    assert ar(vc, s, r, n, M) == ALIAS
+    # ReduceScatter output inside an input
+    r = fake(n, 2 << 40)
+    r[1] = s[0] + 128
+    assert rs(vc, s, r, n, M) == ALIAS
+    # ReduceScatter output exactly at its own input is not in-place-safe
+    assert rs(vc, s, list(s), n, M) == ALIAS
+    # AllGather output over a shard
+    shards = fake(n, 3 << 40)
+    r = fake(n, 2 << 40)
+    r[0] = shards[3] - 64
+    assert ag(vc, shards, r, n, M) == ALIAS
+    # inputs may overlap each other (read only)
+    s2 = [s[0]] * n
+    assert ar(vc, s2, fake(n, 2 << 40), n, M) == CUDA
+    # adjacent but disjoint ranges are fine
+    r = [(2 << 40) + k * bytes_m for k in range(n)]
+    assert ar(vc, s, r, n, M) == CUDA
+
+
+def test_decomposed_alias_rules(vc):
+    n, M = 4, 1000
+    s, z, r = fake(n, 1 << 40), fake(n, 3 << 40), fake(n, 2 << 40)
+    assert dec(vc, s, z, r, n, M) == CUDA
+    assert dec(vc, s, z, list(s), n, M) == CUDA  # in place
+    z2 = list(z)
+    z2[1] = r[2] + 16
+    assert dec(vc, s, z2, r, n, M) == ALIAS
+    z2 = list(z)
+    z2[0] = s[0]
+    assert dec(vc, s, z2, r, n, M) == ALIAS
+    z2 = list(z)
+    z2[3] = z2[2]
+    assert dec(vc, s, z2, r, n, M) == ALIAS
+
+
+def test_oversized_count_rejected(vc):
+    s, r = fake(2, 1 << 40), fake(2, 2 << 40)
+    assert ar(vc, s, r, 2, 1 << 62, dt=I64) == INVALID
+
+
+def test_launch_failure_surfaces_as_cuda_error(vc):
+    s, z, r = fake(4, 1 << 40), fake(4, 3 << 40), fake(4, 2 << 40)
+    assert rs(vc, s, z, 4, 100) == CUDA
+    assert ag(vc, z, r, 4, 100) == CUDA
+    assert ar(vc, s, r, 4, 100) == CUDA
+    assert dec(vc, s, z, r, 4, 100) == CUDA
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from allreduce_reducescatter_allgather_gb300 import _binding
+    monkeypatch.setattr(_binding, "LIB_PATH", tmp_path / "missing" / "libvc.so")
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="CUDA library missing"):
+        _binding.lib()
+
+
+def test_element_misaligned_pointer_rejected(vc):
+    """A buffer not aligned to its element size is rejected on the host (the
+    element-wise kernel paths would otherwise access it misaligned)."""
+    s, r = fake(4, 1 << 40), fake(4, 2 << 40)
+    s[1] += 2
+    assert ar(vc, s, r, 4, 100, dt=F32) == INVALID
+    assert ar(vc, s, r, 4, 100, dt=BF16) == CUDA  # 2-byte aligned is enough for bf16
+    r[0] += 4
+    assert rs(vc, fake(4, 1 << 40), r, 4, 100, dt=I64) == INVALID
+    assert ag(vc, fake(4, 1 << 40), r, 4, 100, dt=I32) == CUDA

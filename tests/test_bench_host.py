@@ -1,0 +1,54 @@
+"""Host-side logic of bench.py on CPU: the byte accounting of a step and the
+max-over-ranks / sum-over-ranks aggregation, the latter with two gloo ranks."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def test_step_bytes():
+    n, M, s = 4, 67_108_864, 4
+    b = bench.step_bytes(n, M, s)
+    assert b["reduce_scatter"] == n * M * s + M * s
+    assert b["all_gather"] == M * s + n * M * s
+    assert b["fused_ar"] == 2 * n * M * s
+    assert b["step"] == 4 * n * M * s + 2 * M * s
+
+
+def _free_port():
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, total = bench.aggregate(torch, 10.0 + 5 * rank, 1000 * (rank + 1), world)
+        q.put((rank, ms, total))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, ms, total in got:
+        assert ms == 15.0          # the slower rank's time
+        assert total == 3000       # every rank's bytes

@@ -1,0 +1,522 @@
+"""Parity of the CUDA collectives with the CPU oracle, through the C ABI.
+
+Integers, and floats in the same order as the oracle, must match bit for bit;
+a float result in a different order must lie within the bound the tests name.
+Small and medium cases compare every element of every output; the full-size
+four-rank 256 MiB workload compares a million sampled indices (plus every
+chunk boundary) one by one, and checks properties that hold at any size on
+the device.  Output buffers carry guard elements after their end that must
+come back untouched.
+"""
+from __future__ import annotations
+
+import math
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from conftest import ints, read_golden
+from gpu_util import assert_bits_equal, bits, to_device, to_host, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+ORDERS = ["ring", "recursive_halving", "pairwise_tree"]
+OPS = ["sum", "prod", "max", "min", "avg"]
+GUARD = 32  # guard elements after every output buffer
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import allreduce_reducescatter_allgather_gb300 as vc
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    return SimpleNamespace(torch=torch, vc=vc, dev=dev)
+
+
+def orders_for(n):
+    return ORDERS if n & (n - 1) == 0 else ["ring"]
+
+
+def sentinel(dtype):
+    return {"int32": -77, "int64": -77, "float32": 12345.0, "bfloat16": 77.0}[dtype]
+
+
+class Guarded:
+    """N device buffers of `numel` elements, each followed by GUARD sentinel
+    elements inside the same allocation, optionally starting `offset`
+    elements into it (a misaligned base)."""
+
+    def __init__(self, env, n, numel, dtype, offset=0):
+        torch = env.torch
+        self.dtype = dtype
+        self.bigs = []
+        self.views = []
+        for _ in range(n):
+            big = torch.full((offset + numel + GUARD,), sentinel(dtype),
+                             dtype=torch_dtype(torch, dtype), device=env.dev)
+            self.bigs.append(big)
+            self.views.append(big[offset:offset + numel])
+        self.offset, self.numel = offset, numel
+
+    def check_guards(self, env):
+        for big in self.bigs:
+            tail = big[self.offset + self.numel:]
+            assert env.torch.all(tail == sentinel(self.dtype)).item(), "guard overwritten"
+
+    def host(self):
+        return [to_host(v, self.dtype) for v in self.views]
+
+
+def run_all_paths(env, xs, dtype, op, order, offset=0):
+    """RS, AG (of the GPU's own shards), fused AR and decomposed AR."""
+    vc = env.vc
+    n, M = len(xs), xs[0].size
+    q = vc.vc_shard_count(M, n)
+    d = to_device(env.torch, xs, dtype, env.dev, offset=offset)
+    z = Guarded(env, n, q, dtype, offset)
+    g = Guarded(env, n, M, dtype, offset)
+    y = Guarded(env, n, M, dtype, offset)
+    s2 = Guarded(env, n, q, dtype, offset)
+    y2 = Guarded(env, n, M, dtype, offset)
+    vc.vc_reduce_scatter(d, z.views, op=op, order=order)
+    vc.vc_all_gather(z.views, g.views)
+    vc.vc_all_reduce(d, y.views, op=op, order=order)
+    vc.vc_all_reduce_decomposed(d, s2.views, y2.views, op=op, order=order)
+    env.torch.cuda.synchronize()
+    for b in (z, g, y, s2, y2):
+        b.check_guards(env)
+    return SimpleNamespace(rs=z.host(), ag=g.host(), ar=y.host(), dec_shards=s2.host(),
+                           dec=y2.host())
+
+
+def check_all_paths(res, xs, dtype, op, order, tag=""):
+    n = len(xs)
+    oz = oracle.reduce_scatter(xs, dtype, op, order)
+    oy = oracle.all_reduce(xs, dtype, op, order)
+    og = oracle.all_gather(res.rs, xs[0].size, dtype)  # AG on its own, from the GPU's shards
+    for r in range(n):
+        t = f"{tag} {dtype} {op} {order} rank {r}"
+        assert_bits_equal(res.rs[r], oz[r], dtype, "RS " + t)
+        assert_bits_equal(res.dec_shards[r], oz[r], dtype, "decomposed shards " + t)
+        assert_bits_equal(res.ar[r], oy[r], dtype, "AR " + t)
+        assert_bits_equal(res.dec[r], oy[r], dtype, "decomposed AR " + t)
+        assert_bits_equal(res.ag[r], og[r], dtype, "AG " + t)
+
+
+def gen(dtype, n, M, seed):
+    if dtype in ("float32", "bfloat16"):
+        return si.generate(dtype, "uniform_pm1", n, M, seed=seed)
+    return si.generate(dtype, "uniform_int", n, M, seed=seed, lo=-100, hi=100)
+
+
+# ------------------------------------------------- the pages' contracts --
+
+@pytest.mark.parametrize("order", ORDERS)
+def test_worked_example(env, order):
+    """Four ranks, twenty int64, 100r + i: 600 + 4i, shards of five, every
+    path and op ("NCCL 专家课程 07", 一个四 rank 手算例子)."""
+    g = read_golden("worked_example_n4_m20_int64.txt")
+    xs = si.generate("int64", "rank_linear", 4, 20, seed=0)
+    res = run_all_paths(env, xs, "int64", "sum", order)
+    expect = np.array(ints(g["allreduce"]), np.int64)
+    for r in range(4):
+        np.testing.assert_array_equal(res.ar[r], expect)
+        np.testing.assert_array_equal(res.dec[r], expect)
+        np.testing.assert_array_equal(res.rs[r], np.array(ints(g[f"shard{r}"]), np.int64))
+    for op in OPS:
+        check_all_paths(run_all_paths(env, xs, "int64", op, order), xs, "int64", op, order)
+
+
+def test_negative_contracts(env):
+    """A rolled gather and RS(MAX)+AG both differ from AR(SUM) on the GPU's
+    own results (条件一, 条件二)."""
+    vc, torch = env.vc, env.torch
+    xs = si.generate("int64", "rank_linear", 4, 20, seed=0)
+    d = to_device(torch, xs, "int64", env.dev)
+    direct = [torch.empty_like(t) for t in d]
+    vc.vc_all_reduce(d, direct, op="sum")
+    zmax = [torch.empty(5, dtype=torch.int64, device=env.dev) for _ in range(4)]
+    gmax = [torch.empty_like(t) for t in d]
+    vc.vc_reduce_scatter(d, zmax, op="max")
+    vc.vc_all_gather(zmax, gmax)
+    zsum = [torch.empty(5, dtype=torch.int64, device=env.dev) for _ in range(4)]
+    gsum = [torch.empty_like(t) for t in d]
+    vc.vc_reduce_scatter(d, zsum, op="sum")
+    vc.vc_all_gather(zsum, gsum)
+    torch.cuda.synchronize()
+    assert torch.equal(direct[0], gsum[0])
+    rolled = gsum[0].reshape(4, -1).roll(1, dims=0).reshape(-1)
+    assert not torch.equal(direct[0], rolled)
+    assert not torch.equal(direct[0], gmax[0])
+
+
+def test_padding_contract(env):
+    """M = 1003 on four ranks: shards of 251, RS + AG trimmed equals the direct
+    AR; an unpadded 250-element output is rejected before any kernel runs and
+    stays untouched (Contract 实验四)."""
+    vc, torch = env.vc, env.torch
+    g = read_golden("padding_m1003_n4.txt")
+    n, M = int(g["n"]), int(g["M"])
+    xs = si.generate("int64", "rank_linear", n, M, seed=0)
+    res = run_all_paths(env, xs, "int64", "sum", "ring")
+    assert all(z.size == int(g["q"]) for z in res.rs)
+    for r in range(n):
+        np.testing.assert_array_equal(res.dec[r], res.ar[r])
+    check_all_paths(res, xs, "int64", "sum", "ring")
+    d = to_device(torch, xs, "int64", env.dev)
+    bad = [torch.full((int(g["unpadded_output"]),), 7, dtype=torch.int64, device=env.dev)
+           for _ in range(n)]
+    with pytest.raises(ValueError, match="ceil"):
+        vc.vc_reduce_scatter(d, bad)
+    torch.cuda.synchronize()
+    assert all(torch.all(b == 7).item() for b in bad)
+
+
+def test_max_is_not_zero_padded(env):
+    """MAX over all-negative int64 with M % N != 0: the shard tail holds the
+    dtype minimum and matches the identity-padded oracle, not a zero pad."""
+    vc, torch = env.vc, env.torch
+    n, M = 4, 19
+    xs = [-(100 * r + np.arange(M, dtype=np.int64)) - 1 for r in range(n)]
+    res = run_all_paths(env, xs, "int64", "max", "ring")
+    check_all_paths(res, xs, "int64", "max", "ring")
+    q = oracle.shard_count(M, n)
+    zero_padded = [np.concatenate([x, np.zeros(n * q - M, np.int64)]) for x in xs]
+    bad = oracle.reduce_scatter(zero_padded, "int64", "max", "ring")
+    assert not np.array_equal(res.rs[-1], bad[-1])
+    assert res.rs[-1][-1] == np.iinfo(np.int64).min
+    del vc, torch
+
+
+# ------------------------------------------------------ workload configs --
+
+@pytest.mark.parametrize("order", ["ring", "recursive_halving", "pairwise_tree"])
+@pytest.mark.parametrize("op", OPS)
+def test_n8_m1000003_fp32(env, op, order):
+    """Eight ranks, 1,000,003 fp32 uniform[-1,1) (q = 125,001, five padding
+    slots, misaligned shard starts): every path bit for bit."""
+    w = si.WORKLOADS["n8_m1000003_f32_uniform"]
+    xs = si.generate(w["dtype"], w["dist"], w["n"], w["M"], seed=w["seed"])
+    if op == "prod":
+        xs = [np.float32(1.0) + x * np.float32(0.125) for x in xs]
+    res = run_all_paths(env, xs, "float32", op, order)
+    check_all_paths(res, xs, "float32", op, order)
+
+
+@pytest.fixture(scope="module")
+def bucket_bf16():
+    w = si.WORKLOADS["n8_bucket25mib_bf16_normal"]
+    return si.generate(w["dtype"], w["dist"], w["n"], w["M"], seed=w["seed"], sigma=w["sigma"])
+
+
+@pytest.mark.parametrize("order", ORDERS)
+def test_gradient_bucket_bf16(env, bucket_bf16, order):
+    """Eight ranks, one 25 MiB bucket of bf16 normal(0, 1e-3): SUM then AVG
+    with fp32 accumulation; RS (ZeRO-style shards) and fused AR bit for bit."""
+    vc, torch = env.vc, env.torch
+    xs = bucket_bf16
+    n, M = len(xs), xs[0].size
+    q = vc.vc_shard_count(M, n)
+    d = to_device(torch, xs, "bfloat16", env.dev)
+    for op in ("sum", "avg"):
+        z = Guarded(env, n, q, "bfloat16")
+        y = Guarded(env, n, M, "bfloat16")
+        vc.vc_reduce_scatter(d, z.views, op=op, order=order)
+        vc.vc_all_reduce(d, y.views, op=op, order=order)
+        torch.cuda.synchronize()
+        z.check_guards(env)
+        y.check_guards(env)
+        oz = oracle.reduce_scatter(xs, "bfloat16", op, order)
+        oy = oracle.all_reduce(xs, "bfloat16", op, order)
+        zh, yh = z.host(), y.host()
+        for r in range(n):
+            assert_bits_equal(zh[r], oz[r], "bfloat16", f"RS {op} {order}")
+        assert_bits_equal(yh[0], oy[0], "bfloat16", f"AR {op} {order}")
+        for r in range(1, n):
+            assert torch.equal(y.views[r], y.views[0])
+
+
+def test_bf16_other_order_within_one_ulp(env, bucket_bf16):
+    """Against an oracle in a different order, bf16 results lie within one
+    bf16 ulp of the fp32-accumulated oracle rounded to bf16."""
+    vc, torch = env.vc, env.torch
+    xs = [x[:2_000_000] for x in bucket_bf16]
+    d = to_device(torch, xs, "bfloat16", env.dev)
+    y = [torch.empty_like(t) for t in d]
+    vc.vc_all_reduce(d, y, op="sum", order="ring")
+    torch.cuda.synchronize()
+    got = to_host(y[0], "bfloat16").astype(np.int32)
+    for order in ("recursive_halving", "pairwise_tree"):
+        ref = oracle.all_reduce(xs, "bfloat16", "sum", order)[0].astype(np.int32)
+        # adjacent bf16 values of one sign differ by 1 in their bit pattern
+        same_sign = (got & 0x8000) == (ref & 0x8000)
+        diff = np.abs(got - ref)
+        ok = (same_sign & (diff <= 1)) | ((got & 0x7FFF) == 0) & ((ref & 0x7FFF) <= 1) \
+            | ((ref & 0x7FFF) == 0) & ((got & 0x7FFF) <= 1)
+        assert np.all(ok), order
+
+
+def _sample_indices(rng, limit, q, n, K):
+    idx = rng.integers(0, limit, size=K, dtype=np.int64)
+    edges = []
+    for c in range(n + 1):
+        for off in (-2, -1, 0, 1, 2):
+            edges.append(c * q + off)
+    edges += [limit - 1, limit - 2]
+    edges = np.array([e for e in edges if 0 <= e < limit], np.int64)
+    return np.unique(np.concatenate([idx, edges]))
+
+
+def _check_sampled(env, d, y0, z, dtype, op, order, K=1 << 20, seed=0):
+    """Compare sampled AR outputs (y0) and RS shards (z) with the oracle
+    reducing those indices one by one from the device's own input bytes."""
+    torch = env.torch
+    n, M = len(d), d[0].numel()
+    q = env.vc.vc_shard_count(M, n)
+    rng = np.random.default_rng(seed)
+    # AllReduce indices
+    idx = _sample_indices(rng, M, q, n, K)
+    ti = torch.from_numpy(idx).to(env.dev)
+    xs_at = [to_host(t[ti], dtype) for t in d]
+    want = oracle.reduce_points(xs_at, idx, n, M, dtype, op, order)
+    assert_bits_equal(to_host(y0[ti], dtype), want, dtype, f"sampled AR {dtype} {op} {order}")
+    # ReduceScatter indices over the padded range [0, N*q)
+    idx = _sample_indices(rng, n * q, q, n, K // 4)
+    safe = torch.from_numpy(np.minimum(idx, M - 1)).to(env.dev)
+    xs_at = [to_host(t[safe], dtype) for t in d]
+    want = oracle.reduce_points(xs_at, idx, n, M, dtype, op, order)
+    flat = torch.cat([zz for zz in z])
+    got = to_host(flat[torch.from_numpy(idx).to(env.dev)], dtype)
+    assert_bits_equal(got, want, dtype, f"sampled RS {dtype} {op} {order}")
+
+
+@pytest.mark.parametrize("name", ["n4_256mib_f32_normal", "n4_m67108864_i64_uniform"])
+def test_full_size_four_ranks(env, name):
+    """Four ranks of 67,108,864 elements (fp32 normal, int64 uniform): fused
+    AR, RS and decomposed AR at full size in the bench's launch configuration;
+    a million sampled indices against the oracle, and on the device: all AR
+    outputs identical, AR == decomposed AR, RS shard r == AR[rq : rq+q]."""
+    vc, torch = env.vc, env.torch
+    w = dict(si.WORKLOADS[name])
+    dtype = w.pop("dtype")
+    d = si.generate_device(torch, dtype, w.pop("dist"), w.pop("n"), w.pop("M"),
+                           w.pop("seed"), env.dev, **w)
+    n, M = len(d), d[0].numel()
+    q = vc.vc_shard_count(M, n)
+    for order in ORDERS:
+        y = [torch.empty_like(t) for t in d]
+        z = [torch.empty(q, dtype=d[0].dtype, device=env.dev) for _ in range(n)]
+        s2 = [torch.empty(q, dtype=d[0].dtype, device=env.dev) for _ in range(n)]
+        y2 = [torch.empty_like(t) for t in d]
+        vc.vc_all_reduce(d, y, op="sum", order=order)
+        vc.vc_reduce_scatter(d, z, op="sum", order=order)
+        vc.vc_all_reduce_decomposed(d, s2, y2, op="sum", order=order)
+        torch.cuda.synchronize()
+        for r in range(n):
+            assert torch.equal(y[r], y[0])
+            assert torch.equal(y2[r], y[0])
+            assert torch.equal(s2[r], z[r])
+            assert torch.equal(z[r], y[0][r * q:(r + 1) * q])
+        _check_sampled(env, d, y[0], z, dtype, "sum", order, seed=ORDERS.index(order))
+        del y, z, s2, y2
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- the sweep --
+
+SWEEP_DTYPES = ["int32", "int64", "float32", "bfloat16"]
+SWEEP_OPS = ["sum", "max", "min", "prod"]
+
+
+def _sweep_cases(max_bytes):
+    cases = []
+    k = 0
+    for dtype in SWEEP_DTYPES:
+        es = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}[dtype]
+        for n in (2, 4, 8, 16, 64):
+            for nbytes in [8192 * 4 ** j for j in range(9)] + [1 << 30]:
+                if nbytes > max_bytes or n * nbytes > (64 << 30):
+                    continue
+                op = SWEEP_OPS[k % 4]
+                order = ORDERS[(k // 4) % 3]
+                k += 1
+                cases.append((dtype, n, nbytes // es, op, order))
+    return cases
+
+
+@pytest.mark.parametrize("dtype,n,M,op,order", _sweep_cases(512 << 10))
+def test_sweep_full_compare(env, dtype, n, M, op, order):
+    """Per-rank sizes 8 KiB .. 512 KiB, N in {2, 4, 8, 16, 64}, four dtypes,
+    ops and orders cycled: every path, every element."""
+    xs = gen(dtype, n, M, seed=1000 + n + M)
+    if op == "prod" and dtype in ("float32", "bfloat16"):
+        xs = gen_prod_floats(dtype, n, M)
+    res = run_all_paths(env, xs, dtype, op, order)
+    check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M}")
+
+
+def gen_prod_floats(dtype, n, M):
+    # factors near 1 keep long products finite
+    xs = si.generate("float32", "uniform_pm1", n, M, seed=n * 7 + M)
+    xs = [np.float32(1.0) + x * np.float32(1.0 / 64) for x in xs]
+    if dtype == "bfloat16":
+        import torch
+        return [torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+                for x in xs]
+    return xs
+
+
+LARGE = [("float32", 2, 1 << 28), ("bfloat16", 16, 1 << 28), ("int32", 64, 1 << 25),
+         ("int64", 8, 1 << 26), ("float32", 64, 1 << 28)]
+
+
+@pytest.mark.parametrize("dtype,n,M", LARGE)
+def test_sweep_large_sampled(env, dtype, n, M):
+    """Large sweep points (up to 1 GiB per rank, and 64 ranks x 1 GiB): RS and
+    in-place AR, sampled indices against the oracle, outputs identical."""
+    vc, torch = env.vc, env.torch
+    dist = "uniform_pm1" if dtype in ("float32", "bfloat16") else "uniform_int"
+    kw = {} if dist == "uniform_pm1" else {"lo": -100, "hi": 100}
+    d = si.generate_device(torch, dtype, dist, n, M, seed=7 + n, device=env.dev, **kw)
+    q = vc.vc_shard_count(M, n)
+    order = "pairwise_tree" if dtype == "bfloat16" else "ring"
+    z = [torch.empty(q, dtype=d[0].dtype, device=env.dev) for _ in range(n)]
+    vc.vc_reduce_scatter(d, z, op="sum", order=order)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(n)
+    idx = _sample_indices(rng, n * q, q, n, 1 << 16)
+    safe = torch.from_numpy(np.minimum(idx, M - 1)).to(env.dev)
+    xs_at = [to_host(t[safe], dtype) for t in d]
+    want = oracle.reduce_points(xs_at, idx, n, M, dtype, "sum", order)
+    got = to_host(torch.cat(z)[torch.from_numpy(idx).to(env.dev)], dtype)
+    assert_bits_equal(got, want, dtype, "sampled RS")
+    del z
+    # the in-place AR overwrites the inputs: keep the operands of the probes
+    probe = _sample_indices(rng, M, q, n, 1 << 16)
+    tp = torch.from_numpy(probe).to(env.dev)
+    xs_probe = [to_host(t[tp], dtype) for t in d]
+    vc.vc_all_reduce(d, None, op="sum", order=order)
+    torch.cuda.synchronize()
+    want = oracle.reduce_points(xs_probe, probe, n, M, dtype, "sum", order)
+    for r in (0, n // 2, n - 1):
+        assert_bits_equal(to_host(d[r][tp], dtype), want, dtype, f"in-place AR rank {r}")
+    for r in range(1, n):
+        assert torch.equal(d[r], d[0])
+    del d
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ edge cases --
+
+EDGE_NM = [(1, 1), (1, 37), (2, 1), (2, 3), (3, 2), (3, 7), (4, 3), (4, 5), (5, 1), (7, 6),
+           (7, 15), (8, 7), (8, 9), (8, 33), (13, 12), (13, 200), (16, 17), (32, 31),
+           (63, 1000), (64, 63), (64, 65), (64, 1031)]
+
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_edge_shapes(env, dtype, offset):
+    """Tiny and ragged shapes (M < N, M = N +- 1, odd q, every residue of M
+    and q modulo the vector width), N = 1 and N = 64, and bases one element
+    off 16-byte alignment: every path, every element."""
+    k = 0
+    for n, M in EDGE_NM:
+        for order in orders_for(n):
+            op = OPS[k % len(OPS)]
+            k += 1
+            xs = gen(dtype, n, M, seed=n * 1000 + M)
+            res = run_all_paths(env, xs, dtype, op, order, offset=offset)
+            check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M} off={offset}")
+
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+def test_residues(env, dtype):
+    """M and q in every residue class modulo the vector width, N = 4 and 8."""
+    V = {"int32": 4, "int64": 2, "float32": 4, "bfloat16": 8}[dtype]
+    for n in (4, 8):
+        for M in range(n * 64, n * 64 + n * V + 1):
+            xs = gen(dtype, n, M, seed=M)
+            res = run_all_paths(env, xs, dtype, "sum", "ring")
+            check_all_paths(res, xs, dtype, "sum", "ring", tag=f"N={n} M={M}")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "int64", "bfloat16"])
+def test_in_place(env, dtype):
+    """In-place AR and in-place decomposed AR (recvbufs = sendbufs)."""
+    vc, torch = env.vc, env.torch
+    n, M = 8, 100_003
+    xs = gen(dtype, n, M, seed=3)
+    for order in ORDERS:
+        oy = oracle.all_reduce(xs, dtype, "sum", order)
+        d = to_device(torch, xs, dtype, env.dev)
+        vc.vc_all_reduce(d, None, op="sum", order=order)
+        d2 = to_device(torch, xs, dtype, env.dev)
+        q = vc.vc_shard_count(M, n)
+        sh = [torch.empty(q, dtype=d2[0].dtype, device=env.dev) for _ in range(n)]
+        vc.vc_all_reduce_decomposed(d2, sh, None, op="sum", order=order)
+        torch.cuda.synchronize()
+        for r in range(n):
+            assert_bits_equal(to_host(d[r], dtype), oy[r], dtype, f"in-place AR {order}")
+            assert_bits_equal(to_host(d2[r], dtype), oy[r], dtype, f"in-place dec {order}")
+
+
+def test_all_gather_from_arbitrary_shards(env):
+    """AG alone, from shards that are not RS outputs, with misaligned shard
+    bases and q not a multiple of the vector width."""
+    vc, torch = env.vc, env.torch
+    for dtype in SWEEP_DTYPES:
+        for n, M in ((3, 1000), (8, 1_000_003), (64, 4099)):
+            q = vc.vc_shard_count(M, n)
+            zs = gen(dtype, n, q, seed=q)
+            for off in (0, 1):
+                dz = to_device(torch, zs, dtype, env.dev, offset=off)
+                y = Guarded(env, n, M, dtype)
+                vc.vc_all_gather(dz, y.views)
+                torch.cuda.synchronize()
+                y.check_guards(env)
+                want = oracle.all_gather(zs, M, dtype)
+                yh = y.host()
+                for r in range(n):
+                    assert_bits_equal(yh[r], want[r], dtype, f"AG {dtype} N={n} off={off}")
+
+
+@pytest.mark.parametrize("n", [8, 64])
+def test_fp32_other_order_within_bound(env, n):
+    """Against the oracle in another order, fp32 sums satisfy
+    |gpu - oracle| <= 2 N 2^-24 sum_s |x^(s)_i|."""
+    vc, torch = env.vc, env.torch
+    M = 200_003
+    xs = si.generate("float32", "uniform_pm1", n, M, seed=n)
+    d = to_device(torch, xs, "float32", env.dev)
+    absum = sum(np.abs(x.astype(np.float64)) for x in xs)
+    for order in ORDERS:
+        y = [torch.empty_like(t) for t in d]
+        vc.vc_all_reduce(d, y, op="sum", order=order)
+        torch.cuda.synchronize()
+        got = to_host(y[0], "float32").astype(np.float64)
+        for other in ORDERS + ["sequential"]:
+            ref = oracle.all_reduce(xs, "float32", "sum", other)[0].astype(np.float64)
+            assert np.all(np.abs(got - ref) <= 2 * n * 2.0 ** -24 * absum), (order, other)
+
+
+def test_user_stream(env):
+    """Calls enqueue on the stream they are given."""
+    vc, torch = env.vc, env.torch
+    n, M = 4, 1 << 20
+    xs = gen("float32", n, M, seed=5)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d = to_device(torch, xs, "float32", env.dev)
+        y = [torch.empty_like(t) for t in d]
+        vc.vc_all_reduce(d, y, op="sum", order="ring", stream=s)
+    s.synchronize()
+    oy = oracle.all_reduce(xs, "float32", "sum", "ring")
+    assert_bits_equal(to_host(y[0], "float32"), oy[0], "float32", "stream")
