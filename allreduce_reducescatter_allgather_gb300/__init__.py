@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     vc_all_gather,
     vc_all_reduce,
     vc_all_reduce_decomposed,
+    vc_all_reduce_decomposed_noalloc,
     vc_reduce_scatter,
     vc_shard_count,
 )

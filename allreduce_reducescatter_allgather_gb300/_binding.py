@@ -28,7 +28,7 @@ MAX_RANKS = 64
 
 # Every function the header declares (checked by the tests against vc.h).
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
-           "vc_all_reduce_decomposed", "vc_status_string")
+           "vc_all_reduce_decomposed", "vc_all_reduce_decomposed_noalloc", "vc_status_string")
 
 
 class VcError(RuntimeError):
@@ -202,3 +202,55 @@ def vc_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum"
     check_status(lib().vc_all_reduce_decomposed(_ptrs(sendbufs), _ptrs(shardbufs),
                                                 _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
                                                 ORDERS[order], _stream(stream, dev)))
+
+
+# ------------------------------------------------ no-allocation variant --
+
+# Size of the library's static shard scratch (VC_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
+_ESIZE = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}
+
+
+def noalloc_scratch_needed(count: int, nranks: int, dtype: str) -> int:
+    """Bytes of shard scratch a call needs: N shards of ceil(count/N)
+    elements, each rounded up to 256 bytes."""
+    q = -(-count // nranks)
+    return nranks * (-(-q * _ESIZE[dtype] // 256) * 256)
+
+
+def vc_all_reduce_decomposed_noalloc(sendbufs, recvbufs=None, op: str = "sum",
+                                     order: str = "ring", stream=None):
+    """The decomposed AllReduce (ReduceScatter, then AllGather) for callers
+    that cannot allocate device memory where they call it -- code whose
+    memory a framework's allocator owns and budgets, latency-critical paths
+    that cannot pay for cudaMalloc, plugins handed only their buffers.  The
+    N intermediate shards live in a 32 MiB scratch array inside the library
+    instead of caller buffers; the call allocates nothing.  Same bits as
+    vc_all_reduce_decomposed.  recvbufs=None reduces in place.
+
+    The first call on a device looks up the scratch array's address; make it
+    before any stream capture.  Calls share the array: calls that overlap on
+    the GPU race.  Raises ValueError when the shards do not fit."""
+    n = len(sendbufs)
+    recvbufs = list(sendbufs) if recvbufs is None else recvbufs
+    if len(recvbufs) != n:
+        raise ValueError("one output buffer per rank")
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    need = noalloc_scratch_needed(M, n, dt)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"{n} shards of {vc_shard_count(M, n)} {dt} elements need {need} bytes "
+                         f"of scratch; the library's static scratch holds "
+                         f"{NOALLOC_SCRATCH_BYTES} bytes (use vc_all_reduce_decomposed with "
+                         f"caller-allocated shards)")
+    L = lib()
+    fn = L.vc_all_reduce_decomposed_noalloc
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    fn.argtypes = [vpp, vpp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    check_status(fn(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order],
+                    _stream(stream, dev)))

@@ -21,7 +21,7 @@ LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "libvc.so"
 
 SOURCES = ["vc_api.cu", "vc_reduce_f32.cu", "vc_reduce_bf16.cu", "vc_reduce_i32.cu",
-           "vc_reduce_i64.cu"]
+           "vc_reduce_i64.cu", "vc_noalloc.cu"]
 HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

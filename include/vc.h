@@ -167,6 +167,44 @@ vc_status_t vc_all_reduce_decomposed(const void *const *sendbufs, void *const *s
                                      vc_dtype_t dtype, vc_op_t op, vc_order_t order,
                                      vc_stream_t stream);
 
+/* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
+ * 32 MiB on every GPU that loads this library, held until the process exits. */
+#define VC_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* The decomposed AllReduce for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point: the pages' collectives
+ * always work on buffers the framework has allocated.
+ *
+ * Some callers cannot call cudaMalloc where they need the AllReduce: code
+ * whose device memory is owned and budgeted by a framework's caching
+ * allocator (a raw cudaMalloc would bypass the budget), latency-critical
+ * paths that cannot afford cudaMalloc/cudaFree and the synchronisation they
+ * imply, or plugins that are handed only their input and output buffers.
+ * vc_all_reduce_decomposed needs N shard buffers from its caller; this
+ * variant keeps them instead in a scratch array compiled into the library,
+ * so the caller passes only sendbufs and recvbufs (same meaning, layout and
+ * in-place rule as vc_all_reduce_decomposed) and gets the same bits.  The
+ * call allocates nothing.
+ *
+ * Limit: each of the N shards (q = vc_shard_count(count, nranks) elements)
+ * is rounded up to a multiple of 256 bytes, and together they must fit in
+ * VC_NOALLOC_SCRATCH_BYTES; a larger count returns VC_ERR_INVALID_ARGUMENT
+ * and launches nothing.  (A 25 MiB gradient bucket fits.)
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.
+ *
+ * Sharing: every call uses the same array, which keeps the shards of the
+ * last call.  Nothing in it needs to start at zero: the ReduceScatter writes
+ * every shard element, padding included, before the AllGather reads it.
+ * Calls that overlap on the GPU (on different streams, or from host threads
+ * that do not order their streams) race on the array and corrupt each
+ * other's results; serialise them. */
+vc_status_t vc_all_reduce_decomposed_noalloc(const void *const *sendbufs, void *const *recvbufs,
+                                             int nranks, size_t count, vc_dtype_t dtype,
+                                             vc_op_t op, vc_order_t order, vc_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *vc_status_string(vc_status_t status);
 

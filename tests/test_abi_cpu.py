@@ -53,7 +53,8 @@ def header_functions():
 def test_header_declares_the_entry_points():
     names = header_functions()
     assert names == sorted(["vc_shard_count", "vc_reduce_scatter", "vc_all_gather",
-                            "vc_all_reduce", "vc_all_reduce_decomposed", "vc_status_string"])
+                            "vc_all_reduce", "vc_all_reduce_decomposed",
+                            "vc_all_reduce_decomposed_noalloc", "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -234,3 +235,23 @@ def test_element_misaligned_pointer_rejected(vc):
     r[0] += 4
     assert rs(vc, fake(4, 1 << 40), r, 4, 100, dt=I64) == INVALID
     assert ag(vc, fake(4, 1 << 40), r, 4, 100, dt=I32) == CUDA
+
+
+def test_noalloc_checks(vc):
+    """The no-allocation AllReduce validates like the others and rejects
+    shards that do not fit its static scratch, before touching the GPU."""
+    from allreduce_reducescatter_allgather_gb300._binding import NOALLOC_SCRATCH_BYTES
+    L = vc.lib()
+
+    def na(send, recv, n, M, dt=F32, op=SUM, order=RING):
+        return L.vc_all_reduce_decomposed_noalloc(table(vc, send), table(vc, recv), n, M, dt,
+                                                  op, order, None)
+    s, r = fake(4, 1 << 40), fake(4, 2 << 40)
+    assert na(s, r, 4, NOALLOC_SCRATCH_BYTES // 4 + 1) == INVALID
+    assert na(s, r, 4, 0) == SUCCESS
+    assert na(s, r, 0, 100) == INVALID
+    assert na(s, r, 3, 100, order=RH) == UNSUPPORTED
+    r2 = list(r)
+    r2[1] = s[2]
+    assert na(s, r2, 4, 100) == ALIAS
+    assert na(s, list(s), 4, 100) == CUDA  # valid, in place: the launch hook fires
