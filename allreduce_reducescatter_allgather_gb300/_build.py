@@ -20,9 +20,15 @@ BUILD = PKG / "_build"
 LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "libvc.so"
 
-SOURCES = ["vc_api.cu", "vc_reduce_f32.cu", "vc_reduce_bf16.cu", "vc_reduce_i32.cu",
-           "vc_reduce_i64.cu", "vc_noalloc.cu"]
+SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu"]
 HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
+# vc_reduce_inst.cu compiled once per (element type, op): (object, -D flags)
+INSTANCE_SOURCE = "vc_reduce_inst.cu"
+_TYPES = {"i32": "int32_t", "i64": "long long", "f32": "float", "bf16": "__nv_bfloat16"}
+_OPS = {"sum": "OpSum", "prod": "OpProd", "max": "OpMax", "min": "OpMin"}
+INSTANCES = [(f"vc_reduce_{t}_{o}", [f"-DVC_T={ct}", f"-DVC_OP={op}",
+                                     f"-DVC_FN=launch_reduce_{t}_{o}"])
+             for t, ct in _TYPES.items() for o, op in _OPS.items()]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
@@ -43,7 +49,8 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES + HEADERS] + [INCLUDE / "vc.h", Path(__file__)]
+    deps = [CSRC / s for s in SOURCES + HEADERS + [INSTANCE_SOURCE]] + [INCLUDE / "vc.h",
+                                                                       Path(__file__)]
     return any(d.stat().st_mtime > t for d in deps)
 
 
@@ -55,18 +62,24 @@ def build_library(force: bool = False, jobs: int | None = None) -> Path:
     BUILD.mkdir(exist_ok=True)
     LIBDIR.mkdir(exist_ok=True)
 
-    def compile_one(src: str):
-        obj = BUILD / (Path(src).stem + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-I", str(INCLUDE), "-c", str(CSRC / src), "-o", str(obj)]
+    def compile_one(job):
+        stem, src, defines = job
+        obj = BUILD / (stem + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *defines, "-I", str(INCLUDE), "-c", str(CSRC / src), "-o",
+               str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
-        (BUILD / (Path(src).stem + ".ptxas.log")).write_text(r.stdout + r.stderr)
+        (BUILD / (stem + ".ptxas.log")).write_text(r.stdout + r.stderr)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr[-4000:]}")
+            raise RuntimeError(f"nvcc failed on {stem}:\n{r.stderr[-4000:]}")
         return obj
 
-    jobs = jobs or min(len(SOURCES), os.cpu_count() or 4)
+    jobs_list = [(Path(s).stem, s, []) for s in SOURCES]
+    jobs_list += [(stem, INSTANCE_SOURCE, defs) for stem, defs in INSTANCES]
+    # the largest slices first, so the pool finishes together
+    jobs_list.sort(key=lambda j: 0 if j[1] == INSTANCE_SOURCE else 1)
+    jobs = jobs or max(1, os.cpu_count() or 4)
     with ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+        objs = list(ex.map(compile_one, jobs_list))
     tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", str(tmp), *map(str, objs),

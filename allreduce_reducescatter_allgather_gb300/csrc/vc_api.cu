@@ -4,7 +4,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
-#include <unordered_map>
 
 #include "vc.h"
 #include "vc_device.cuh"
@@ -147,15 +146,14 @@ vc_status_t launch_all_gather(const void* const* in, void* const* out, int n, si
 
 }  // namespace
 
-// Grid size for the grid-stride kernels: one block per 256 vectors, capped
-// at the blocks that fit on all SMs at once (queried once per kernel).
-int grid_blocks(const void* kernel, long long nvec) {
+// Grid size for the grid-stride kernels: one block per kThreads units, at
+// most kWaves blocks per SM (the SM count is queried once per device).
+int grid_blocks(long long units) {
     static std::mutex mu;
-    static std::unordered_map<const void*, int> per_sm;
     static int sm_count[VC_MAX_RANKS] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= VC_MAX_RANKS) return -1;
-    int occ = 0, sms = 0;
+    int sms = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (sm_count[dev] == 0) {
@@ -165,41 +163,21 @@ int grid_blocks(const void* kernel, long long nvec) {
             sm_count[dev] = v;
         }
         sms = sm_count[dev];
-        auto it = per_sm.find(kernel);
-        if (it == per_sm.end()) {
-            int v = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kThreads, 0) !=
-                cudaSuccess)
-                return -1;
-            it = per_sm.emplace(kernel, v < 1 ? 1 : v).first;
-        }
-        occ = it->second;
     }
-    const long long want = (nvec + kThreads - 1) / kThreads;
-    const long long cap = (long long)sms * occ;
-    long long b = want < cap ? want : cap;
+    const long long want = (units + kThreads - 1) / kThreads;
+    const long long cap = (long long)sms * kWaves;
+    const long long b = want < cap ? want : cap;
     return (int)(b < 1 ? 1 : b);
 }
 
 cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st) {
     const long long nvec = (p.M * esize + 15) / 16;
-    int blocks;
+    const int blocks = grid_blocks((nvec + kGatherSlots - 1) / kGatherSlots);
+    if (blocks < 1) return cudaErrorInvalidConfiguration;
     switch (esize) {
-    case 2:
-        blocks = grid_blocks((const void*)vc_ag_kernel<2>, nvec);
-        if (blocks < 1) return cudaErrorInvalidConfiguration;
-        vc_ag_kernel<2><<<blocks, kThreads, 0, st>>>(p);
-        break;
-    case 4:
-        blocks = grid_blocks((const void*)vc_ag_kernel<4>, nvec);
-        if (blocks < 1) return cudaErrorInvalidConfiguration;
-        vc_ag_kernel<4><<<blocks, kThreads, 0, st>>>(p);
-        break;
-    case 8:
-        blocks = grid_blocks((const void*)vc_ag_kernel<8>, nvec);
-        if (blocks < 1) return cudaErrorInvalidConfiguration;
-        vc_ag_kernel<8><<<blocks, kThreads, 0, st>>>(p);
-        break;
+    case 2: vc_ag_kernel<2><<<blocks, kThreads, 0, st>>>(p); break;
+    case 4: vc_ag_kernel<4><<<blocks, kThreads, 0, st>>>(p); break;
+    case 8: vc_ag_kernel<8><<<blocks, kThreads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -20,7 +20,10 @@ namespace vc {
 
 constexpr int kMaxRanks = 64;
 constexpr int kThreads = 256;
-constexpr int kGroup = 8;  // loads issued together before they are folded
+constexpr int kGroup = 16;     // loads a streaming fold issues before folding them
+constexpr int kRingGroup = 8;  // the same for the ring with a run-time N (whose
+                               // run-time rank indices cost more registers)
+constexpr int kWaves = 64;  // grid = up to 64 blocks per SM: many more than resident
 
 enum { kOrderRing = 0, kOrderRecursiveHalving = 1, kOrderPairwiseTree = 2 };
 
@@ -138,12 +141,10 @@ __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) {
     *reinterpret_cast<unsigned short*>(p) = (unsigned short)bf16_bits(v);
 }
 
-// Streaming 16-byte accesses: each byte is touched once, so ask the caches
-// to evict it first.
-__device__ __forceinline__ uint4 ld16(const void* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ void st16(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+// 16-byte accesses with the default cache policy (measured faster on GB300
+// than the evict-first streaming hints for these access patterns).
+__device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // ------------------------------------------------------------------- ops --
 
@@ -220,54 +221,106 @@ __device__ __forceinline__ long long avg_div(long long s, int n) { return s / (l
 
 // ------------------------------------------------------------- loaders --
 
-// Loads the 16-byte vector at element offset i0 of rank r.
+// A loader hands the folds one operand at a time: raw(r) fetches rank r's
+// operand in storage form (a 16-byte vector, or one element) and cvt()
+// widens it to accumulator lanes.  The folds fetch a whole group with raw()
+// before widening any of it, so the group's loads are in flight together
+// and only the narrow storage form occupies registers meanwhile.
+
+// The 16-byte vector at element offset i0 of rank r.
 template <class T> struct VecLoader {
     using A = typename Traits<T>::Acc;
-    static constexpr int V = Traits<T>::V;
+    static constexpr int W = Traits<T>::V;
+    using Raw = uint4;
     const ReduceParams& p;
     long long i0;
-    __device__ __forceinline__ Vec<A, V> operator()(int r) const {
-        Vec<A, V> v;
-        unpack(ld16(static_cast<const T*>(p.in[r]) + i0), v, (T*)nullptr);
+    __device__ __forceinline__ Raw raw(int r) const {
+        return ld16(static_cast<const T*>(p.in[r]) + i0);
+    }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& u) const {
+        Vec<A, W> v;
+        unpack(u, v, (T*)nullptr);
         return v;
     }
 };
 
-// Loads one element of the padded logical buffer: x^(r)_i below M, the
-// identity from M to N*q.
+// One element of the padded logical buffer: x^(r)_i below M, the identity
+// from M to N*q.
 template <class T, class Op> struct ScalarLoader {
     using A = typename Traits<T>::Acc;
+    static constexpr int W = 1;
+    using Raw = A;
     const ReduceParams& p;
     long long i;
-    __device__ __forceinline__ Vec<A, 1> operator()(int r) const {
+    __device__ __forceinline__ Raw raw(int r) const {
+        return (i < p.M) ? load1(static_cast<const T*>(p.in[r]) + i) : Identity<T, Op>::get();
+    }
+    __device__ __forceinline__ Vec<A, 1> cvt(const Raw& a) const {
         Vec<A, 1> v;
-        v.x[0] = (i < p.M) ? load1(static_cast<const T*>(p.in[r]) + i) : Identity<T, Op>::get();
+        v.x[0] = a;
         return v;
     }
 };
+
+// The 16-byte vector at element offset i0 of rank r, with the rank's base
+// pointer taken from a copy of the pointer table in shared memory (for folds
+// whose rank index is only known at run time).
+template <class T> struct SharedTableLoader {
+    using A = typename Traits<T>::Acc;
+    static constexpr int W = Traits<T>::V;
+    using Raw = uint4;
+    const void* const* table;
+    long long i0;
+    __device__ __forceinline__ Raw raw(int r) const {
+        return ld16(static_cast<const T*>(table[r]) + i0);
+    }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& u) const {
+        Vec<A, W> v;
+        unpack(u, v, (T*)nullptr);
+        return v;
+    }
+};
+
+// Vectors already loaded into registers: buf[r][u] is rank r's vector for
+// the thread's slot u.
+template <class T, int NR, int U> struct PreLoader {
+    using A = typename Traits<T>::Acc;
+    static constexpr int W = Traits<T>::V;
+    using Raw = uint4;
+    const uint4 (&buf)[NR][U];
+    int u;
+    __device__ __forceinline__ Raw raw(int r) const { return buf[r][u]; }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& x) const {
+        Vec<A, W> v;
+        unpack(x, v, (T*)nullptr);
+        return v;
+    }
+};
+
+template <class L> using VecOf = Vec<typename L::A, L::W>;
 
 // --------------------------------------------------------------- orders --
 
 // Ring: chunk c is started by rank c and every later rank on the ring adds
 // its operand, so the value is the left fold over ranks c, c+1, ..., c+N-1
-// (mod N).  Ranks are visited in groups of kGroup whose loads are all issued
-// before any of them is folded.
-template <class Op, class A, int W, class L>
-__device__ __forceinline__ Vec<A, W> fold_ring(const L& ld, int n, int c) {
-    Vec<A, W> acc;
+// (mod N).  Ranks are visited in groups of kRingGroup whose loads are all
+// issued before any of them is folded.
+template <class Op, class L>
+__device__ __forceinline__ VecOf<L> fold_ring(const L& ld, int n, int c) {
+    VecOf<L> acc;
     int r = c;
 #pragma unroll 1
-    for (int k0 = 0; k0 < n; k0 += kGroup) {
-        Vec<A, W> t[kGroup];
+    for (int k0 = 0; k0 < n; k0 += kRingGroup) {
+        typename L::Raw t[kRingGroup];
 #pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-            if (k0 + u < n) t[u] = ld(r);
+        for (int u = 0; u < kRingGroup; ++u) {
+            if (k0 + u < n) t[u] = ld.raw(r);
             r = (r + 1 == n) ? 0 : r + 1;
         }
-        if (k0 == 0) acc = t[0];
+        if (k0 == 0) acc = ld.cvt(t[0]);
 #pragma unroll
-        for (int u = 0; u < kGroup; ++u)
-            if (k0 + u < n && k0 + u > 0) acc = vop<Op>(acc, t[u]);
+        for (int u = 0; u < kRingGroup; ++u)
+            if (k0 + u < n && k0 + u > 0) acc = vop<Op>(acc, ld.cvt(t[u]));
     }
     return acc;
 }
@@ -275,79 +328,103 @@ __device__ __forceinline__ Vec<A, W> fold_ring(const L& ld, int n, int c) {
 // Recursive halving: the value over ranks {BASE + k*STRIDE : k < CNT} is the
 // value over the even k combined with the value over the odd k (the pairing
 // at distance N/2 happens first, so it sits at the bottom of the tree).
-template <class Op, class A, int W, int KB, int KS, int KC, int G>
-__device__ __forceinline__ Vec<A, W> rh_local(const Vec<A, W> (&t)[G]) {
+template <class Op, int KB, int KS, int KC, class L, class R, int G>
+__device__ __forceinline__ VecOf<L> rh_local(const L& ld, const R (&t)[G]) {
     if constexpr (KC == 1) {
-        return t[KB];
+        return ld.cvt(t[KB]);
     } else {
-        return vop<Op>(rh_local<Op, A, W, KB, 2 * KS, KC / 2>(t),
-                       rh_local<Op, A, W, KB + KS, 2 * KS, KC / 2>(t));
+        return vop<Op>(rh_local<Op, KB, 2 * KS, KC / 2>(ld, t),
+                       rh_local<Op, KB + KS, 2 * KS, KC / 2>(ld, t));
     }
 }
 
-template <class Op, class A, int W, int BASE, int STRIDE, int CNT, class L>
-__device__ __forceinline__ Vec<A, W> rh_group(const L& ld) {
+template <class Op, int BASE, int STRIDE, int CNT, class L>
+__device__ __forceinline__ VecOf<L> rh_group(const L& ld) {
     if constexpr (CNT <= kGroup) {
-        Vec<A, W> t[CNT];
+        typename L::Raw t[CNT];
 #pragma unroll
-        for (int k = 0; k < CNT; ++k) t[k] = ld(BASE + k * STRIDE);
-        return rh_local<Op, A, W, 0, 1, CNT>(t);
+        for (int k = 0; k < CNT; ++k) t[k] = ld.raw(BASE + k * STRIDE);
+        return rh_local<Op, 0, 1, CNT>(ld, t);
     } else {
-        Vec<A, W> lo = rh_group<Op, A, W, BASE, 2 * STRIDE, CNT / 2>(ld);
-        Vec<A, W> hi = rh_group<Op, A, W, BASE + STRIDE, 2 * STRIDE, CNT / 2>(ld);
+        VecOf<L> lo = rh_group<Op, BASE, 2 * STRIDE, CNT / 2>(ld);
+        VecOf<L> hi = rh_group<Op, BASE + STRIDE, 2 * STRIDE, CNT / 2>(ld);
         return vop<Op>(lo, hi);
     }
 }
 
 // Tree: node P at level L (its lowest set bit) has children P - L/2 and
 // P + L/2; its subtree holds ranks P-L+1 .. P+L-1 and its value is
-// (left (+) right) (+) own.  Subtrees of at most 7 ranks are loaded as one
+// (left (+) right) (+) own.  Subtrees of at most 15 ranks are loaded as one
 // group; t[K] holds rank P-L+1+K.
-template <class Op, class A, int W, int K, int L, int G>
-__device__ __forceinline__ Vec<A, W> tree_local(const Vec<A, W> (&t)[G]) {
+template <class Op, int K, int L, class Ld, class R, int G>
+__device__ __forceinline__ VecOf<Ld> tree_local(const Ld& ld, const R (&t)[G]) {
     if constexpr (L == 1) {
-        return t[K];
+        return ld.cvt(t[K]);
     } else {
-        Vec<A, W> kids = vop<Op>(tree_local<Op, A, W, K - L / 2, L / 2>(t),
-                                 tree_local<Op, A, W, K + L / 2, L / 2>(t));
-        return vop<Op>(kids, t[K]);
+        VecOf<Ld> kids = vop<Op>(tree_local<Op, K - L / 2, L / 2>(ld, t),
+                                 tree_local<Op, K + L / 2, L / 2>(ld, t));
+        return vop<Op>(kids, ld.cvt(t[K]));
     }
 }
 
-template <class Op, class A, int W, int P, int L, class Ld>
-__device__ __forceinline__ Vec<A, W> tree_node(const Ld& ld) {
+template <class Op, int P, int L, class Ld>
+__device__ __forceinline__ VecOf<Ld> tree_node(const Ld& ld) {
     if constexpr (L == 1) {
-        return ld(P);
-    } else if constexpr (L <= 4) {
-        Vec<A, W> t[2 * L - 1];
+        return ld.cvt(ld.raw(P));
+    } else if constexpr (2 * L - 1 <= kGroup) {
+        typename Ld::Raw t[2 * L - 1];
 #pragma unroll
-        for (int k = 0; k < 2 * L - 1; ++k) t[k] = ld(P - L + 1 + k);
-        return tree_local<Op, A, W, L - 1, L>(t);
+        for (int k = 0; k < 2 * L - 1; ++k) t[k] = ld.raw(P - L + 1 + k);
+        return tree_local<Op, L - 1, L>(ld, t);
     } else {
-        Vec<A, W> l = tree_node<Op, A, W, P - L / 2, L / 2>(ld);
-        Vec<A, W> r = tree_node<Op, A, W, P + L / 2, L / 2>(ld);
-        return vop<Op>(vop<Op>(l, r), ld(P));
+        VecOf<Ld> l = tree_node<Op, P - L / 2, L / 2>(ld);
+        VecOf<Ld> r = tree_node<Op, P + L / 2, L / 2>(ld);
+        return vop<Op>(vop<Op>(l, r), ld.cvt(ld.raw(P)));
     }
 }
 
 // The root, rank 0, has the single child N/2.
-template <class Op, class A, int W, int N, class Ld>
-__device__ __forceinline__ Vec<A, W> fold_tree(const Ld& ld) {
+template <class Op, int N, class Ld>
+__device__ __forceinline__ VecOf<Ld> fold_tree(const Ld& ld) {
     if constexpr (N == 1) {
-        return ld(0);
+        return ld.cvt(ld.raw(0));
     } else {
-        return vop<Op>(tree_node<Op, A, W, N / 2, N / 2>(ld), ld(0));
+        return vop<Op>(tree_node<Op, N / 2, N / 2>(ld), ld.cvt(ld.raw(0)));
     }
 }
 
-template <class Op, int ORDER, int NT, class A, int W, class L>
-__device__ __forceinline__ Vec<A, W> fold(const L& ld, int n, int c) {
-    if constexpr (ORDER == kOrderRecursiveHalving) {
-        return rh_group<Op, A, W, 0, 1, NT>(ld);
-    } else if constexpr (ORDER == kOrderPairwiseTree) {
-        return fold_tree<Op, A, W, NT>(ld);
+// Ring with N known at compile time: the left fold starting at rank C, with
+// every rank index a constant (operands may already sit in registers).
+template <class Op, int N, int C, class L>
+__device__ __forceinline__ VecOf<L> ring_from(const L& ld) {
+    VecOf<L> acc = ld.cvt(ld.raw(C));
+#pragma unroll
+    for (int k = 1; k < N; ++k) acc = vop<Op>(acc, ld.cvt(ld.raw((C + k) % N)));
+    return acc;
+}
+
+// Picks the rotation for chunk c among the N compile-time ones.
+template <class Op, int N, int C, class L>
+__device__ __forceinline__ VecOf<L> ring_switch(const L& ld, int c) {
+    if constexpr (C == N - 1) {
+        return ring_from<Op, N, C>(ld);
     } else {
-        return fold_ring<Op, A, W>(ld, n, c);
+        if (c == C) return ring_from<Op, N, C>(ld);
+        return ring_switch<Op, N, C + 1>(ld, c);
+    }
+}
+
+// NT > 0: N is a compile-time constant; NT == 0: ring with a run-time N.
+template <class Op, int ORDER, int NT, class L>
+__device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int c) {
+    if constexpr (ORDER == kOrderRecursiveHalving) {
+        return rh_group<Op, 0, 1, NT>(ld);
+    } else if constexpr (ORDER == kOrderPairwiseTree) {
+        return fold_tree<Op, NT>(ld);
+    } else if constexpr (NT > 0) {
+        return ring_switch<Op, NT, 0>(ld, c);
+    } else {
+        return fold_ring<Op>(ld, n, c);
     }
 }
 
@@ -368,6 +445,34 @@ __device__ __forceinline__ int chunk_of(long long i, long long q, float inv_q, i
 
 // --------------------------------------------------------------- kernels --
 
+// The result vector of elements i0 .. i0+V-1 (chunk c) to its destination:
+// AllReduce, all N outputs; ReduceScatter, the shard that owns it.
+template <class T, int NT, bool RS, class A, int V>
+__device__ __forceinline__ void store_result(const ReduceParams& p, int c, long long i0,
+                                             Vec<A, V>& acc) {
+    if (p.avg) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
+    }
+    if constexpr (RS) {
+        T* dst = static_cast<T*>(p.out[c]) + (i0 - (long long)c * p.q);
+        if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+            st16(dst, pack(acc, (T*)nullptr));
+        } else {
+#pragma unroll
+            for (int k = 0; k < V; ++k) store1(dst + k, acc.x[k]);
+        }
+    } else {
+        const uint4 u = pack(acc, (T*)nullptr);
+        if constexpr (NT > 0) {
+#pragma unroll
+            for (int s = 0; s < NT; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
+        } else {
+            for (int s = 0; s < p.n; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
+        }
+    }
+}
+
 // Reduces one element the slow way (misaligned bases, a vector straddling a
 // chunk boundary or the end of the data, or the padding).
 template <class T, class Op, int ORDER, int NT, bool RS>
@@ -375,7 +480,7 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     using A = typename Traits<T>::Acc;
     const int c = chunk_of(i, p.q, p.inv_q, p.n);
     ScalarLoader<T, Op> ld{p, i};
-    Vec<A, 1> v = fold<Op, ORDER, NT, A, 1>(ld, p.n, c);
+    Vec<A, 1> v = fold<Op, ORDER, NT>(ld, p.n, c);
     A r = v.x[0];
     if (p.avg) r = avg_div(r, p.n);
     if constexpr (RS) {
@@ -386,99 +491,200 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     }
 }
 
+// One vector slot on its own: the vector path if it lies inside one chunk
+// and inside the data on aligned bases, else element by element.
 template <class T, class Op, int ORDER, int NT, bool RS>
-__device__ __forceinline__ void reduce_body(const ReduceParams& p) {
-    using A = typename Traits<T>::Acc;
+__device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
     constexpr int V = Traits<T>::V;
+    const long long i0 = v * V;
+    const int c = chunk_of(i0, p.q, p.inv_q, p.n);
+    if (p.vec_ok && i0 + V <= p.M && i0 + V <= (long long)(c + 1) * p.q) {
+        VecLoader<T> ld{p, i0};
+        auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+        store_result<T, NT, RS>(p, c, i0, acc);
+    } else {
+        for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
+    }
+}
+
+// The kernel body.  A block takes U*blockDim.x consecutive vectors per
+// iteration; thread t owns the U vectors t, t + blockDim.x, ... of that
+// range (each warp access is 512 contiguous bytes).  When all U vectors sit
+// inside one chunk and inside the data on aligned bases (nearly always), the
+// thread issues every load before it folds or stores anything:
+//  - N <= 8 (NT > 0): the N x U vectors (at most 16) are loaded into
+//    registers in rank order, with constant rank indices, then folded slot by
+//    slot in the order's tree (the ring picks its rotation by the chunk);
+//  - otherwise (U = 1): the fold streams its operands in groups of kGroup;
+//    the ring with run-time N reads its rotated pointers from shared memory.
+// Anything else goes slot by slot through reduce_slot.
+template <class T, class Op, int ORDER, int NT, int U, bool RS>
+__device__ __forceinline__ void reduce_body(const ReduceParams& p) {
+    constexpr int V = Traits<T>::V;
+    constexpr bool kPre = (NT > 0 && NT <= 8);
+    constexpr bool kTable = (NT == 0);  // ring, run-time N
+    __shared__ const void* s_in[kTable ? kMaxRanks : 1];
+    __shared__ void* s_out[kTable ? kMaxRanks : 1];
+    if constexpr (kTable) {
+        for (int r = threadIdx.x; r < p.n; r += blockDim.x) {
+            s_in[r] = p.in[r];
+            s_out[r] = p.out[r];
+        }
+        __syncthreads();
+    }
     const long long nvec = (p.limit + V - 1) / V;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
-        const long long i0 = v * V;
-        const int c = chunk_of(i0, p.q, p.inv_q, p.n);
-        const long long cend = (long long)(c + 1) * p.q;
-        if (p.vec_ok && i0 + V <= p.M && i0 + V <= cend) {
-            VecLoader<T> ld{p, i0};
-            Vec<A, V> acc = fold<Op, ORDER, NT, A, V>(ld, p.n, c);
-            if (p.avg) {
+    const long long span = (long long)blockDim.x * U;
+    for (long long b0 = (long long)blockIdx.x * span; b0 < nvec; b0 += (long long)gridDim.x * span) {
+        const long long v0 = b0 + threadIdx.x;
+        const long long vlast = v0 + (long long)(U - 1) * blockDim.x;
+        bool wide = false;
+        int c = 0;
+        if (vlast < nvec && p.vec_ok) {
+            c = chunk_of(v0 * V, p.q, p.inv_q, p.n);
+            const long long end = vlast * V + V;
+            wide = end <= p.M && end <= (long long)(c + 1) * p.q;
+        }
+        if (wide) {
+            if constexpr (kPre) {
+                uint4 buf[NT][U];
 #pragma unroll
-                for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
-            }
-            if constexpr (RS) {
-                T* dst = static_cast<T*>(p.out[c]) + (i0 - (long long)c * p.q);
-                if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                    st16(dst, pack(acc, (T*)nullptr));
+                for (int r = 0; r < NT; ++r) {
+                    const T* base = static_cast<const T*>(p.in[r]) + v0 * V;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) buf[r][u] = ld16(base + (long long)u * blockDim.x * V);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    PreLoader<T, NT, U> ld{buf, u};
+                    auto acc = fold<Op, ORDER, NT>(ld, NT, c);
+                    store_result<T, NT, RS>(p, c, (v0 + (long long)u * blockDim.x) * V, acc);
+                }
+            } else if constexpr (kTable) {
+                static_assert(U == 1, "streaming folds take one vector per thread");
+                SharedTableLoader<T> ld{s_in, v0 * V};
+                auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+                if (p.avg) {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
+                }
+                const long long i0 = v0 * V;
+                if constexpr (RS) {
+                    T* dst = static_cast<T*>(s_out[c]) + (i0 - (long long)c * p.q);
+                    if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                        st16(dst, pack(acc, (T*)nullptr));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < V; ++k) store1(dst + k, acc.x[k]);
+                    }
                 } else {
-#pragma unroll
-                    for (int k = 0; k < V; ++k) store1(dst + k, acc.x[k]);
+                    const uint4 u = pack(acc, (T*)nullptr);
+                    for (int s = 0; s < p.n; ++s) st16(static_cast<T*>(s_out[s]) + i0, u);
                 }
             } else {
-                const uint4 u = pack(acc, (T*)nullptr);
-                if constexpr (NT > 0) {
-#pragma unroll
-                    for (int s = 0; s < NT; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
-                } else {
-                    for (int s = 0; s < p.n; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
-                }
+                static_assert(U == 1, "streaming folds take one vector per thread");
+                VecLoader<T> ld{p, v0 * V};
+                auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+                store_result<T, NT, RS>(p, c, v0 * V, acc);
             }
         } else {
-            for (int k = 0; k < V && i0 + k < p.limit; ++k)
-                reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
+#pragma unroll 1
+            for (int u = 0; u < U; ++u) {
+                const long long v = v0 + (long long)u * blockDim.x;
+                if (v < nvec) reduce_slot<T, Op, ORDER, NT, RS>(p, v);
+            }
         }
     }
 }
 
 // ReduceScatter: index space [0, N*q), one store per element into the shard
 // that owns it.
-template <class T, class Op, int ORDER, int NT>
+template <class T, class Op, int ORDER, int NT, int U>
 __global__ void __launch_bounds__(kThreads) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
-    reduce_body<T, Op, ORDER, NT, true>(p);
+    reduce_body<T, Op, ORDER, NT, U, true>(p);
 }
 
 // Fused AllReduce: index space [0, M), N stores per element.
-template <class T, class Op, int ORDER, int NT>
+template <class T, class Op, int ORDER, int NT, int U>
 __global__ void __launch_bounds__(kThreads) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
-    reduce_body<T, Op, ORDER, NT, false>(p);
+    reduce_body<T, Op, ORDER, NT, U, false>(p);
 }
 
 // AllGather: output index i comes from shard s = floor(i/q) at offset i - sq,
 // and is written to all N outputs.  It moves bits only, so it is typed by
-// element size alone.
+// element size alone.  Like the reductions, a thread takes kGatherSlots
+// vectors (blockDim.x apart) and loads all of them before it stores any.
 template <int ES> struct Bits;
 template <> struct Bits<2> { using U = unsigned short; };
 template <> struct Bits<4> { using U = unsigned; };
 template <> struct Bits<8> { using U = unsigned long long; };
 
+constexpr int kGatherSlots = 4;
+
+template <int ES>
+__device__ __forceinline__ uint4 gather_load(const GatherParams& p, int s, long long i0) {
+    using U = typename Bits<ES>::U;
+    constexpr int V = 16 / ES;
+    const U* src = static_cast<const U*>(p.in[s]) + (i0 - (long long)s * p.q);
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) return ld16(src);
+    union {
+        U t[V];
+        uint4 u;
+    } w;
+#pragma unroll
+    for (int k = 0; k < V; ++k) w.t[k] = src[k];
+    return w.u;
+}
+
+template <int ES>
+__device__ __noinline__ void gather_slot(const GatherParams& p, long long v) {
+    using U = typename Bits<ES>::U;
+    constexpr int V = 16 / ES;
+    const long long i0 = v * V;
+    const int s = chunk_of(i0, p.q, p.inv_q, p.n);
+    if (p.vec_ok && i0 + V <= p.M && i0 + V <= (long long)(s + 1) * p.q) {
+        const uint4 val = gather_load<ES>(p, s, i0);
+        for (int r = 0; r < p.n; ++r) st16(static_cast<U*>(p.out[r]) + i0, val);
+    } else {
+        for (int k = 0; k < V && i0 + k < p.M; ++k) {
+            const long long i = i0 + k;
+            const int si = chunk_of(i, p.q, p.inv_q, p.n);
+            const U val = static_cast<const U*>(p.in[si])[i - (long long)si * p.q];
+            for (int r = 0; r < p.n; ++r) static_cast<U*>(p.out[r])[i] = val;
+        }
+    }
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__ GatherParams p) {
     using U = typename Bits<ES>::U;
     constexpr int V = 16 / ES;
+    constexpr int S = kGatherSlots;
     const long long nvec = (p.M + V - 1) / V;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
-        const long long i0 = v * V;
-        const int s = chunk_of(i0, p.q, p.inv_q, p.n);
-        const long long send = (long long)(s + 1) * p.q;
-        if (p.vec_ok && i0 + V <= p.M && i0 + V <= send) {
-            const U* src = static_cast<const U*>(p.in[s]) + (i0 - (long long)s * p.q);
-            uint4 val;
-            if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-                val = ld16(src);
-            } else {
-                union {
-                    U t[V];
-                    uint4 u;
-                } w;
+    const long long span = (long long)blockDim.x * S;
+    for (long long b0 = (long long)blockIdx.x * span; b0 < nvec; b0 += (long long)gridDim.x * span) {
+        const long long v0 = b0 + threadIdx.x;
+        const long long vlast = v0 + (long long)(S - 1) * blockDim.x;
+        bool wide = false;
+        int s = 0;
+        if (vlast < nvec && p.vec_ok) {
+            s = chunk_of(v0 * V, p.q, p.inv_q, p.n);
+            const long long end = vlast * V + V;
+            wide = end <= p.M && end <= (long long)(s + 1) * p.q;
+        }
+        if (wide) {
+            uint4 val[S];
 #pragma unroll
-                for (int k = 0; k < V; ++k) w.t[k] = src[k];
-                val = w.u;
+            for (int u = 0; u < S; ++u) val[u] = gather_load<ES>(p, s, (v0 + (long long)u * blockDim.x) * V);
+            for (int r = 0; r < p.n; ++r) {
+                U* dst = static_cast<U*>(p.out[r]) + v0 * V;
+#pragma unroll
+                for (int u = 0; u < S; ++u) st16(dst + (long long)u * blockDim.x * V, val[u]);
             }
-            for (int r = 0; r < p.n; ++r) st16(static_cast<U*>(p.out[r]) + i0, val);
         } else {
-            for (int k = 0; k < V && i0 + k < p.M; ++k) {
-                const long long i = i0 + k;
-                const int si = chunk_of(i, p.q, p.inv_q, p.n);
-                const U val = static_cast<const U*>(p.in[si])[i - (long long)si * p.q];
-                for (int r = 0; r < p.n; ++r) static_cast<U*>(p.out[r])[i] = val;
+#pragma unroll 1
+            for (int u = 0; u < S; ++u) {
+                const long long v = v0 + (long long)u * blockDim.x;
+                if (v < nvec) gather_slot<ES>(p, v);
             }
         }
     }
@@ -491,8 +697,10 @@ cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int order, bool rs,
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int order, bool rs, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st);
 
-// Blocks for a grid-stride kernel: enough for every vector, at most one
-// full wave of resident blocks on every SM.
-int grid_blocks(const void* kernel, long long nvec);
+// Blocks for a grid-stride kernel over `units` thread-units: enough for
+// every unit, at most kWaves blocks per SM.  (Many more blocks than fit at
+// once keep the blocks in flight on neighbouring addresses, which the HBM
+// serves faster than one resident wave striding over the whole buffer.)
+int grid_blocks(long long units);
 
 }  // namespace vc

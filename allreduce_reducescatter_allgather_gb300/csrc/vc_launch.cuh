@@ -1,62 +1,67 @@
-// Dispatch from run-time (op, order, N) to a kernel instance.  Included once
-// per element type (vc_reduce_<type>.cu) so the instances compile in
-// parallel.
+// Dispatch from a run-time (order, N) to a kernel instance.  Included by
+// vc_reduce_inst.cu, which the build compiles once per (element type, op).
 #pragma once
 
 #include "vc_device.cuh"
 
 namespace vc {
 
-template <class T, class Op, int ORDER, int NT>
+template <class T, class Op, int ORDER, int NT, int U>
 cudaError_t launch_one(const ReduceParams& p, bool rs, cudaStream_t st) {
     constexpr int V = Traits<T>::V;
     const long long nvec = (p.limit + V - 1) / V;
-    if (rs) {
-        const int blocks = grid_blocks((const void*)vc_rs_kernel<T, Op, ORDER, NT>, nvec);
-        if (blocks < 1) return cudaErrorInvalidConfiguration;
-        vc_rs_kernel<T, Op, ORDER, NT><<<blocks, kThreads, 0, st>>>(p);
-    } else {
-        const int blocks = grid_blocks((const void*)vc_ar_kernel<T, Op, ORDER, NT>, nvec);
-        if (blocks < 1) return cudaErrorInvalidConfiguration;
-        vc_ar_kernel<T, Op, ORDER, NT><<<blocks, kThreads, 0, st>>>(p);
-    }
+    const int blocks = grid_blocks((nvec + U - 1) / U);
+    if (blocks < 1) return cudaErrorInvalidConfiguration;
+    if (rs)
+        vc_rs_kernel<T, Op, ORDER, NT, U><<<blocks, kThreads, 0, st>>>(p);
+    else
+        vc_ar_kernel<T, Op, ORDER, NT, U><<<blocks, kThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
-// Recursive halving and the tree are unrolled for N = 2, 4, ..., 64.
+// Up to N = 8 a thread holds all N operands of U vectors in registers (N*U
+// at most 16 vectors of 16 bytes); from N = 9 on it streams one vector's
+// operands at a time.
+template <int N> constexpr int slots_for() { return N <= 4 ? 4 : (N <= 8 ? 2 : 1); }
+
+// Recursive halving and the tree: N = 2, 4, ..., 64.
 template <class T, class Op, int ORDER>
 cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
     switch (p.n) {
-    case 2: return launch_one<T, Op, ORDER, 2>(p, rs, st);
-    case 4: return launch_one<T, Op, ORDER, 4>(p, rs, st);
-    case 8: return launch_one<T, Op, ORDER, 8>(p, rs, st);
-    case 16: return launch_one<T, Op, ORDER, 16>(p, rs, st);
-    case 32: return launch_one<T, Op, ORDER, 32>(p, rs, st);
-    case 64: return launch_one<T, Op, ORDER, 64>(p, rs, st);
+    case 2: return launch_one<T, Op, ORDER, 2, slots_for<2>()>(p, rs, st);
+    case 4: return launch_one<T, Op, ORDER, 4, slots_for<4>()>(p, rs, st);
+    case 8: return launch_one<T, Op, ORDER, 8, slots_for<8>()>(p, rs, st);
+    case 16: return launch_one<T, Op, ORDER, 16, 1>(p, rs, st);
+    case 32: return launch_one<T, Op, ORDER, 32, 1>(p, rs, st);
+    case 64: return launch_one<T, Op, ORDER, 64, 1>(p, rs, st);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+// The ring takes any N: compile-time N up to 8, a run-time N beyond.
+template <class T, class Op>
+cudaError_t launch_ring(const ReduceParams& p, bool rs, cudaStream_t st) {
+    constexpr int R = kOrderRing;
+    switch (p.n) {
+    case 1: return launch_one<T, Op, R, 1, slots_for<1>()>(p, rs, st);
+    case 2: return launch_one<T, Op, R, 2, slots_for<2>()>(p, rs, st);
+    case 3: return launch_one<T, Op, R, 3, slots_for<3>()>(p, rs, st);
+    case 4: return launch_one<T, Op, R, 4, slots_for<4>()>(p, rs, st);
+    case 5: return launch_one<T, Op, R, 5, slots_for<5>()>(p, rs, st);
+    case 6: return launch_one<T, Op, R, 6, slots_for<6>()>(p, rs, st);
+    case 7: return launch_one<T, Op, R, 7, slots_for<7>()>(p, rs, st);
+    case 8: return launch_one<T, Op, R, 8, slots_for<8>()>(p, rs, st);
+    default: return launch_one<T, Op, R, 0, 1>(p, rs, st);
     }
 }
 
 template <class T, class Op>
 cudaError_t launch_order(const ReduceParams& p, int order, bool rs, cudaStream_t st) {
     // With one rank every order is the identity fold: a copy.
-    if (p.n == 1 || order == kOrderRing) return launch_one<T, Op, kOrderRing, 0>(p, rs, st);
+    if (p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
     if (order == kOrderRecursiveHalving)
         return launch_pow2<T, Op, kOrderRecursiveHalving>(p, rs, st);
     return launch_pow2<T, Op, kOrderPairwiseTree>(p, rs, st);
-}
-
-// op: 0 sum, 1 prod, 2 max, 3 min, 4 avg (the sum kernel with p.avg set)
-template <class T>
-cudaError_t launch_reduce_t(const ReduceParams& p, int op, int order, bool rs, cudaStream_t st) {
-    switch (op) {
-    case 0:
-    case 4: return launch_order<T, OpSum>(p, order, rs, st);
-    case 1: return launch_order<T, OpProd>(p, order, rs, st);
-    case 2: return launch_order<T, OpMax>(p, order, rs, st);
-    case 3: return launch_order<T, OpMin>(p, order, rs, st);
-    default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace vc
