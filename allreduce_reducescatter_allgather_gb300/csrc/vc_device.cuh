@@ -303,23 +303,25 @@ template <class L> using VecOf = Vec<typename L::A, L::W>;
 
 // Ring: chunk c is started by rank c and every later rank on the ring adds
 // its operand, so the value is the left fold over ranks c, c+1, ..., c+N-1
-// (mod N).  Ranks are visited in groups of kRingGroup whose loads are all
-// issued before any of them is folded.
-template <class Op, class L>
-__device__ __forceinline__ VecOf<L> fold_ring(const L& ld, int n, int c) {
+// (mod N).  Ranks are visited in groups (kGroup with a compile-time N,
+// kRingGroup otherwise) whose loads are all issued before any is folded.
+template <class Op, int NS, class L>
+__device__ __forceinline__ VecOf<L> fold_ring(const L& ld, int n_rt, int c) {
+    const int n = NS > 0 ? NS : n_rt;  // NS > 0: N known at compile time
+    constexpr int G = NS > 0 ? kGroup : kRingGroup;
     VecOf<L> acc;
     int r = c;
 #pragma unroll 1
-    for (int k0 = 0; k0 < n; k0 += kRingGroup) {
-        typename L::Raw t[kRingGroup];
+    for (int k0 = 0; k0 < n; k0 += G) {
+        typename L::Raw t[G];
 #pragma unroll
-        for (int u = 0; u < kRingGroup; ++u) {
+        for (int u = 0; u < G; ++u) {
             if (k0 + u < n) t[u] = ld.raw(r);
             r = (r + 1 == n) ? 0 : r + 1;
         }
         if (k0 == 0) acc = ld.cvt(t[0]);
 #pragma unroll
-        for (int u = 0; u < kRingGroup; ++u)
+        for (int u = 0; u < G; ++u)
             if (k0 + u < n && k0 + u > 0) acc = vop<Op>(acc, ld.cvt(t[u]));
     }
     return acc;
@@ -415,16 +417,18 @@ __device__ __forceinline__ VecOf<L> ring_switch(const L& ld, int c) {
 }
 
 // NT > 0: N is a compile-time constant; NT == 0: ring with a run-time N.
+// The ring switches among its rotations up to N = 8 and folds in groups
+// with run-time rank indices beyond.
 template <class Op, int ORDER, int NT, class L>
 __device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int c) {
     if constexpr (ORDER == kOrderRecursiveHalving) {
         return rh_group<Op, 0, 1, NT>(ld);
     } else if constexpr (ORDER == kOrderPairwiseTree) {
         return fold_tree<Op, NT>(ld);
-    } else if constexpr (NT > 0) {
+    } else if constexpr (NT > 0 && NT <= 8) {
         return ring_switch<Op, NT, 0>(ld, c);
     } else {
-        return fold_ring<Op>(ld, n, c);
+        return fold_ring<Op, NT>(ld, n, c);
     }
 }
 
@@ -522,7 +526,8 @@ template <class T, class Op, int ORDER, int NT, int U, bool RS>
 __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
     constexpr int V = Traits<T>::V;
     constexpr bool kPre = (NT > 0 && NT <= 8);
-    constexpr bool kTable = (NT == 0);  // ring, run-time N
+    // ring beyond 8 ranks: rotated rank indices read from shared memory
+    constexpr bool kTable = (ORDER == kOrderRing && (NT == 0 || NT > 8));
     __shared__ const void* s_in[kTable ? kMaxRanks : 1];
     __shared__ void* s_out[kTable ? kMaxRanks : 1];
     if constexpr (kTable) {

@@ -38,7 +38,8 @@ cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
     }
 }
 
-// The ring takes any N: compile-time N up to 8, a run-time N beyond.
+// The ring takes any N: compile-time N up to 8 and for 16, 32, 64; a
+// run-time N otherwise.
 template <class T, class Op>
 cudaError_t launch_ring(const ReduceParams& p, bool rs, cudaStream_t st) {
     constexpr int R = kOrderRing;
@@ -51,6 +52,9 @@ cudaError_t launch_ring(const ReduceParams& p, bool rs, cudaStream_t st) {
     case 6: return launch_one<T, Op, R, 6, slots_for<6>()>(p, rs, st);
     case 7: return launch_one<T, Op, R, 7, slots_for<7>()>(p, rs, st);
     case 8: return launch_one<T, Op, R, 8, slots_for<8>()>(p, rs, st);
+    case 16: return launch_one<T, Op, R, 16, 1>(p, rs, st);
+    case 32: return launch_one<T, Op, R, 32, 1>(p, rs, st);
+    case 64: return launch_one<T, Op, R, 64, 1>(p, rs, st);
     default: return launch_one<T, Op, R, 0, 1>(p, rs, st);
     }
 }

@@ -510,6 +510,8 @@ def main(argv=None):
     ap.add_argument("--op", default="sum", choices=["sum", "prod", "max", "min", "avg"])
     ap.add_argument("--order", default="ring",
                     choices=["ring", "recursive_halving", "pairwise_tree"])
+    ap.add_argument("--elements", type=int, default=0,
+                    help="override the elements per rank (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -517,7 +519,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    workload = si.WORKLOADS[args.workload]
+    workload = dict(si.WORKLOADS[args.workload])
+    if args.elements > 0:
+        workload["M"] = args.elements
     if args.impl == "reference":
         return run_reference(args, workload)
     if dist_info()[0] == 1:
