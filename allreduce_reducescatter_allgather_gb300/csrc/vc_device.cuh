@@ -379,9 +379,43 @@ __device__ __forceinline__ VecOf<Ld> tree_node(const Ld& ld) {
         for (int k = 0; k < 2 * L - 1; ++k) t[k] = ld.raw(P - L + 1 + k);
         return tree_local<Op, L - 1, L>(ld, t);
     } else {
+        // the node's own operand is fetched first, so its load is in flight
+        // with the subtrees' loads (the combine order is unchanged)
+        const typename Ld::Raw own = ld.raw(P);
         VecOf<Ld> l = tree_node<Op, P - L / 2, L / 2>(ld);
         VecOf<Ld> r = tree_node<Op, P + L / 2, L / 2>(ld);
-        return vop<Op>(vop<Op>(l, r), ld.cvt(ld.raw(P)));
+        return vop<Op>(vop<Op>(l, r), ld.cvt(own));
+    }
+}
+
+// Trees over 16 or more ranks are read in blocks of 16 consecutive ranks.
+// Block b holds the whole subtree of node 16b+8 (ranks 16b+1 .. 16b+15) and
+// the operand of rank 16b, a node of level 16 or more.  The nodes above the
+// blocks are evaluated eagerly in post-order, so only a few partial results
+// are live at a time; each block hands its first rank's operand up to the
+// node that consumes it.
+template <class Op, int B, class Ld>
+__device__ __forceinline__ VecOf<Ld> tree_block(const Ld& ld, typename Ld::Raw& first) {
+    typename Ld::Raw t[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t[k] = ld.raw(16 * B + k);
+    first = t[0];
+    return tree_local<Op, 8, 8>(ld, t);  // t[k] holds rank 16B + k
+}
+
+// T(P) for a node of level L >= 8.  `first` receives the operand of the
+// lowest rank the subtree's blocks cover, P - L (a node above this one).
+// The right child's blocks start at rank P itself, so the operand they hand
+// back is this node's own.
+template <class Op, int P, int L, class Ld>
+__device__ __forceinline__ VecOf<Ld> tree_upper(const Ld& ld, typename Ld::Raw& first) {
+    if constexpr (L == 8) {
+        return tree_block<Op, (P - 8) / 16>(ld, first);
+    } else {
+        typename Ld::Raw own;
+        VecOf<Ld> l = tree_upper<Op, P - L / 2, L / 2>(ld, first);
+        VecOf<Ld> r = tree_upper<Op, P + L / 2, L / 2>(ld, own);
+        return vop<Op>(vop<Op>(l, r), ld.cvt(own));
     }
 }
 
@@ -390,8 +424,13 @@ template <class Op, int N, class Ld>
 __device__ __forceinline__ VecOf<Ld> fold_tree(const Ld& ld) {
     if constexpr (N == 1) {
         return ld.cvt(ld.raw(0));
+    } else if constexpr (N >= 16) {
+        typename Ld::Raw own0;
+        VecOf<Ld> t = tree_upper<Op, N / 2, N / 2>(ld, own0);
+        return vop<Op>(t, ld.cvt(own0));
     } else {
-        return vop<Op>(tree_node<Op, N / 2, N / 2>(ld), ld.cvt(ld.raw(0)));
+        const typename Ld::Raw own = ld.raw(0);
+        return vop<Op>(tree_node<Op, N / 2, N / 2>(ld), ld.cvt(own));
     }
 }
 
