@@ -17,6 +17,8 @@ from ._binding import (  # noqa: F401
     vc_all_reduce,
     vc_all_reduce_decomposed,
     vc_all_reduce_decomposed_noalloc,
+    vc_broadcast,
+    vc_reduce,
     vc_reduce_scatter,
     vc_shard_count,
 )

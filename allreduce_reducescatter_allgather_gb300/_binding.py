@@ -28,7 +28,8 @@ MAX_RANKS = 64
 
 # Every function the header declares (checked by the tests against vc.h).
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
-           "vc_all_reduce_decomposed", "vc_all_reduce_decomposed_noalloc", "vc_status_string")
+           "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast",
+           "vc_all_reduce_decomposed_noalloc", "vc_status_string")
 
 
 class VcError(RuntimeError):
@@ -59,8 +60,10 @@ def lib() -> ctypes.CDLL:
         L.vc_all_gather.argtypes = [vpp, vpp, i32, sz, i32, vp]
         L.vc_all_reduce.argtypes = [vpp, vpp, i32, sz, i32, i32, i32, vp]
         L.vc_all_reduce_decomposed.argtypes = [vpp, vpp, vpp, i32, sz, i32, i32, i32, vp]
+        L.vc_reduce.argtypes = [vpp, vp, i32, sz, i32, i32, i32, vp]
+        L.vc_broadcast.argtypes = [vp, vpp, i32, sz, i32, vp]
         for f in ("vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
-                  "vc_all_reduce_decomposed"):
+                  "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast"):
             getattr(L, f).restype = i32
         L.vc_status_string.argtypes = [i32]
         L.vc_status_string.restype = ctypes.c_char_p
@@ -202,6 +205,31 @@ def vc_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum"
     check_status(lib().vc_all_reduce_decomposed(_ptrs(sendbufs), _ptrs(shardbufs),
                                                 _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
                                                 ORDERS[order], _stream(stream, dev)))
+
+
+def vc_reduce(sendbufs, recvbuf, op: str = "sum", order: str = "ring", stream=None):
+    """recvbuf <- elementwise reduction of all sendbufs (the AllReduce value,
+    written once, to the root's buffer; recvbuf may be one of sendbufs)."""
+    n = len(sendbufs)
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbuf", [recvbuf], dt, M, dev)
+    check_status(lib().vc_reduce(_ptrs(sendbufs), ctypes.c_void_p(recvbuf.data_ptr()), n, M,
+                                 DTYPES[dt], OPS[op], ORDERS[order], _stream(stream, dev)))
+
+
+def vc_broadcast(sendbuf, recvbufs, stream=None):
+    """recvbufs[r] <- sendbuf for every r (one of recvbufs may be sendbuf)."""
+    n = len(recvbufs)
+    dt = _dtype_name(sendbuf)
+    M = sendbuf.numel()
+    dev = sendbuf.device
+    _check_tensors("sendbuf", [sendbuf], dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    check_status(lib().vc_broadcast(ctypes.c_void_p(sendbuf.data_ptr()), _ptrs(recvbufs), n, M,
+                                    DTYPES[dt], _stream(stream, dev)))
 
 
 # ------------------------------------------------ no-allocation variant --

@@ -92,19 +92,26 @@ bool injected_launch_failure() {
     return v != nullptr && v[0] != '\0' && v[0] != '0';
 }
 
+// nout: outputs the AllReduce kernel writes (n, or 1 for Reduce); the
+// ReduceScatter kernel always has n.
 vc_status_t launch_reduce(const void* const* in, void* const* out, int n, size_t count,
                           vc_dtype_t dtype, vc_op_t op, vc_order_t order, bool rs,
-                          cudaStream_t st) {
+                          cudaStream_t st, int nout = -1) {
     ReduceParams p;
     memset(&p, 0, sizeof p);
     const long long M = (long long)count;
     const long long q = (long long)vc_shard_count(count, n);
+    if (nout < 0) nout = n;
     bool vec = true;
     for (int r = 0; r < n; ++r) {
         p.in[r] = in[r];
-        p.out[r] = out[r];
-        vec = vec && aligned16(in[r]) && (rs || aligned16(out[r]));
+        vec = vec && aligned16(in[r]);
     }
+    for (int r = 0; r < (rs ? n : nout); ++r) {
+        p.out[r] = out[r];
+        vec = vec && (rs || aligned16(out[r]));
+    }
+    p.nout = nout;
     p.M = M;
     p.q = q;
     p.limit = rs ? (long long)n * q : M;
@@ -138,6 +145,29 @@ vc_status_t launch_all_gather(const void* const* in, void* const* out, int n, si
     p.q = (long long)vc_shard_count(count, n);
     p.inv_q = 1.0f / (float)p.q;
     p.n = n;
+    p.vec_ok = vec;
+    if (injected_launch_failure()) return VC_ERR_CUDA;
+    const cudaError_t e = launch_gather(p, elem_size(dtype), st);
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+}
+
+// Broadcast: every output receives the source buffer; the AllGather kernel
+// with a single shard of q = M elements.
+vc_status_t launch_broadcast(const void* src, void* const* out, int nout, size_t count,
+                             vc_dtype_t dtype, cudaStream_t st) {
+    if (nout == 0) return VC_SUCCESS;
+    GatherParams p;
+    memset(&p, 0, sizeof p);
+    bool vec = true;
+    p.in[0] = src;
+    for (int r = 0; r < nout; ++r) {
+        p.out[r] = out[r];
+        vec = vec && aligned16(out[r]);
+    }
+    p.M = (long long)count;
+    p.q = (long long)count;
+    p.inv_q = 1.0f / (float)p.q;
+    p.n = nout;
     p.vec_ok = vec;
     if (injected_launch_failure()) return VC_ERR_CUDA;
     const cudaError_t e = launch_gather(p, elem_size(dtype), st);
@@ -263,6 +293,53 @@ vc_status_t vc_all_reduce_decomposed(const void* const* sendbufs, void* const* s
     if (s != VC_SUCCESS) return s;
     return launch_all_gather(const_cast<const void* const*>(shardbufs), recvbufs, nranks, count,
                              dtype, st);
+}
+
+vc_status_t vc_reduce(const void* const* sendbufs, void* recvbuf, int nranks, size_t count,
+                      vc_dtype_t dtype, vc_op_t op, vc_order_t order, vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
+    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (count == 0) return VC_SUCCESS;
+    if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    void* const out[1] = {recvbuf};
+    if ((s = check_table(out, 1, dtype)) != VC_SUCCESS) return s;
+    // the output may be exactly one rank's input (in place at the root)
+    const Range o = range_of(recvbuf, bm);
+    for (int r = 0; r < nranks; ++r)
+        if (overlap(o, range_of(sendbufs[r], bm)) && sendbufs[r] != recvbuf) return VC_ERR_ALIAS;
+    int same = 0;
+    for (int r = 0; r < nranks; ++r) same += (sendbufs[r] == recvbuf);
+    if (same > 1) return VC_ERR_ALIAS;  // would be read as two ranks and written
+    return launch_reduce(sendbufs, out, nranks, count, dtype, op, order, false,
+                         static_cast<cudaStream_t>(stream), 1);
+}
+
+vc_status_t vc_broadcast(const void* sendbuf, void* const* recvbufs, int nranks, size_t count,
+                         vc_dtype_t dtype, vc_stream_t stream) {
+    size_t bm, bq;
+    vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
+    if (s != VC_SUCCESS) return s;
+    if (count == 0) return VC_SUCCESS;
+    const void* const src[1] = {sendbuf};
+    if ((s = check_table(src, 1, dtype)) != VC_SUCCESS) return s;
+    if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
+    // outputs pairwise disjoint; one of them may be the source itself (the
+    // root's own buffer), which is then left as it is
+    void* outs[VC_MAX_RANKS];
+    int nout = 0;
+    const Range in = range_of(sendbuf, bm);
+    for (int r = 0; r < nranks; ++r) {
+        const Range o = range_of(recvbufs[r], bm);
+        for (int t = 0; t < r; ++t)
+            if (overlap(o, range_of(recvbufs[t], bm))) return VC_ERR_ALIAS;
+        if (recvbufs[r] == sendbuf) continue;
+        if (overlap(o, in)) return VC_ERR_ALIAS;
+        outs[nout++] = recvbufs[r];
+    }
+    return launch_broadcast(sendbuf, outs, nout, count, dtype, static_cast<cudaStream_t>(stream));
 }
 
 const char* vc_status_string(vc_status_t status) {

@@ -38,17 +38,19 @@ struct ReduceParams {
     long long limit;  // index space: N*q for ReduceScatter, M for AllReduce
     float inv_q;      // 1/q, for the chunk estimate
     int n;            // ranks
+    int nout;         // outputs the AllReduce kernel writes: n (AllReduce) or 1 (Reduce)
     int avg;          // divide the sum by n (AVG)
     int vec_ok;       // every base the vector path touches is 16-byte aligned
 };
 
+// AllGather, and Broadcast as an AllGather of one shard of q = M elements.
 struct GatherParams {
     const void* in[kMaxRanks];  // shards, q elements each
     void* out[kMaxRanks];       // outputs, M elements each
     long long M;
     long long q;
     float inv_q;
-    int n;
+    int n;       // outputs written (and shards read, for AllGather)
     int vec_ok;  // every output base 16-byte aligned
 };
 
@@ -509,9 +511,10 @@ __device__ __forceinline__ void store_result(const ReduceParams& p, int c, long 
         const uint4 u = pack(acc, (T*)nullptr);
         if constexpr (NT > 0) {
 #pragma unroll
-            for (int s = 0; s < NT; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
+            for (int s = 0; s < NT; ++s)
+                if (s < p.nout) st16(static_cast<T*>(p.out[s]) + i0, u);
         } else {
-            for (int s = 0; s < p.n; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
+            for (int s = 0; s < p.nout; ++s) st16(static_cast<T*>(p.out[s]) + i0, u);
         }
     }
 }
@@ -529,8 +532,7 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     if constexpr (RS) {
         store1(static_cast<T*>(p.out[c]) + (i - (long long)c * p.q), r);
     } else {
-        const int n = NT ? NT : p.n;
-        for (int s = 0; s < n; ++s) store1(static_cast<T*>(p.out[s]) + i, r);
+        for (int s = 0; s < p.nout; ++s) store1(static_cast<T*>(p.out[s]) + i, r);
     }
 }
 
@@ -622,7 +624,7 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
                     }
                 } else {
                     const uint4 u = pack(acc, (T*)nullptr);
-                    for (int s = 0; s < p.n; ++s) st16(static_cast<T*>(s_out[s]) + i0, u);
+                    for (int s = 0; s < p.nout; ++s) st16(static_cast<T*>(s_out[s]) + i0, u);
                 }
             } else {
                 static_assert(U == 1, "streaming folds take one vector per thread");
@@ -647,7 +649,8 @@ __global__ void __launch_bounds__(kThreads) vc_rs_kernel(const __grid_constant__
     reduce_body<T, Op, ORDER, NT, U, true>(p);
 }
 
-// Fused AllReduce: index space [0, M), N stores per element.
+// Fused AllReduce: index space [0, M), N stores per element (one, to the
+// root's buffer, for Reduce).
 template <class T, class Op, int ORDER, int NT, int U>
 __global__ void __launch_bounds__(kThreads) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, false>(p);

@@ -121,6 +121,7 @@ extern "C" vc_status_t vc_all_reduce_decomposed_noalloc(const void* const* sendb
     rp.limit = (long long)nranks * (long long)q;
     rp.inv_q = gp.inv_q = 1.0f / (float)q;
     rp.n = gp.n = nranks;
+    rp.nout = nranks;
     rp.avg = (op == VC_AVG);
     rp.vec_ok = in_vec;
     gp.vec_ok = out_vec;

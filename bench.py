@@ -431,7 +431,9 @@ def e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, step_bytes_):
 def memory_report(torch, vc, d, args, dev):
     """Peak device memory (MiB above the baseline) of the buffer lifetimes of
     "NCCL 专家课程 07" 显存实验, with all N virtual ranks on one GPU: inputs
-    are copies of the workload made inside each measurement."""
+    are copies of the workload made inside each measurement.  The page's
+    optimised lifetime frees the input after a synchronize; the stream-
+    ordered one (lifetimes.all_reduce_decomposed_low_peak) needs none."""
     n, M = len(d), d[0].numel()
     q = vc.vc_shard_count(M, n)
     MiB = float(1 << 20)
@@ -491,10 +493,16 @@ def memory_report(torch, vc, d, args, dev):
         del shard
         return gathered
 
+    def rs_ag_stream_ordered():
+        from allreduce_reducescatter_allgather_gb300 import lifetimes
+        return lifetimes.all_reduce_decomposed_low_peak([t.clone() for t in d], op=args.op,
+                                                        order=args.order)
+
     for name, fn in (("allreduce_in_place", ar_in_place),
                      ("allreduce_out_of_place", ar_out_of_place),
                      ("reduce_scatter_only", rs_only), ("rs_ag_naive", rs_ag_naive),
-                     ("rs_ag_optimized", rs_ag_optimized)):
+                     ("rs_ag_optimized", rs_ag_optimized),
+                     ("rs_ag_stream_ordered", rs_ag_stream_ordered)):
         measure(name, fn)
     return out
 

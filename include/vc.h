@@ -167,6 +167,25 @@ vc_status_t vc_all_reduce_decomposed(const void *const *sendbufs, void *const *s
                                      vc_dtype_t dtype, vc_op_t op, vc_order_t order,
                                      vc_stream_t stream);
 
+/* Reduce: the AllReduce value of every element, written to one buffer only
+ * (the root's): y_i = (+)_s x^(s)_i for 0 <= i < count, in `order`, with the
+ * same bits vc_all_reduce gives ("通信与互联（01）" 二.1, reduce with root 0;
+ * 二.2: all_reduce = reduce + broadcast).  sendbufs[s]: device buffers of
+ * `count` elements; recvbuf: device buffer of `count` elements, which may be
+ * exactly one of the inputs (the root reducing in place) and must not
+ * otherwise overlap them. */
+vc_status_t vc_reduce(const void *const *sendbufs, void *recvbuf, int nranks, size_t count,
+                      vc_dtype_t dtype, vc_op_t op, vc_order_t order, vc_stream_t stream);
+
+/* Broadcast: recvbufs[r][i] = sendbuf[i] for every r and 0 <= i < count
+ * ("通信与互联（01）" 二.1, broadcast from root 0).  sendbuf: the root's
+ * device buffer of `count` elements; recvbufs: nranks device buffers of
+ * `count` elements, pairwise disjoint.  One of them may be sendbuf itself
+ * (the root's own buffer), which is left as it is; no other may overlap it.
+ * Moves bits only. */
+vc_status_t vc_broadcast(const void *sendbuf, void *const *recvbufs, int nranks, size_t count,
+                         vc_dtype_t dtype, vc_stream_t stream);
+
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
  * 32 MiB on every GPU that loads this library, held until the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -72,12 +72,15 @@ def lib():
         L.oracle_all_reduce_decomposed.argtypes = [vpp, vpp, vpp, i32, i64, i32, i32, i32]
         L.oracle_reduce_points.argtypes = [vpp, ctypes.c_void_p, i64, i32, i64, i32, i32, i32,
                                            ctypes.c_void_p]
+        L.oracle_reduce.argtypes = [vpp, ctypes.c_void_p, i32, i64, i32, i32, i32]
+        L.oracle_broadcast.argtypes = [ctypes.c_void_p, vpp, i32, i64, i32]
         L.oracle_bf16_round.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64]
         L.oracle_bf16_round.restype = None
         L.oracle_tree_parents.argtypes = [i32, ctypes.c_void_p]
         for f in ("oracle_identity", "oracle_reduce_scatter", "oracle_all_gather",
                   "oracle_all_reduce", "oracle_all_reduce_decomposed",
-                  "oracle_reduce_points", "oracle_tree_parents"):
+                  "oracle_reduce_points", "oracle_tree_parents", "oracle_reduce",
+                  "oracle_broadcast"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -156,6 +159,24 @@ def all_reduce_decomposed(xs, dtype: str, op: str, order: str):
     _check(lib().oracle_all_reduce_decomposed(_ptrs(xs), _ptrs(zs), _ptrs(ys), n, M,
                                               DTYPES[dtype], OPS[op], ORDERS[order]))
     return zs, ys
+
+
+def reduce(xs, dtype: str, op: str, order: str):
+    """The AllReduce value, written once (the root's buffer)."""
+    xs = _as_inputs(xs, dtype)
+    n, M = len(xs), xs[0].size
+    y = np.empty(M, NP_STORAGE[dtype])
+    _check(lib().oracle_reduce(_ptrs(xs), y.ctypes.data, n, M, DTYPES[dtype], OPS[op],
+                               ORDERS[order]))
+    return y
+
+
+def broadcast(x, n: int, dtype: str):
+    """N copies of the root's buffer."""
+    x = _as_inputs([x], dtype)[0]
+    ys = [np.empty(x.size, NP_STORAGE[dtype]) for _ in range(n)]
+    _check(lib().oracle_broadcast(x.ctypes.data, _ptrs(ys), n, x.size, DTYPES[dtype]))
+    return ys
 
 
 def reduce_points(xs_at, idx, n: int, M: int, dtype: str, op: str, order: str):

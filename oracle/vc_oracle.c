@@ -454,6 +454,31 @@ int oracle_all_reduce_decomposed(const void *const *x, void *const *shards, void
     return oracle_all_gather((const void *const *)shards, y, n, M, dtype);
 }
 
+/* Reduce to one buffer (the root's): y_i = (+)_s x^(s)_i, the AllReduce
+ * value of every element ("通信与互联（01）" 二.1, reduce with root 0). */
+int oracle_reduce(const void *const *x, void *y, int n, int64_t M, int dtype, int op, int order)
+{
+    plan_t pl;
+    int rc = plan_init(&pl, n, M, dtype, op, order);
+    if (rc != OR_OK)
+        return rc;
+    for (int64_t i = 0; i < M; ++i)
+        store(dtype, y, i, reduce_index(&pl, x, i));
+    return OR_OK;
+}
+
+/* Broadcast from the root's buffer: y^(r)_i = x_i for every r (same page,
+ * broadcast with root 0). */
+int oracle_broadcast(const void *x, void *const *y, int n, int64_t M, int dtype)
+{
+    if (n < 1 || n > OR_MAX_RANKS || M < 0 || elem_size(dtype) == 0)
+        return OR_BAD_ARGUMENT;
+    for (int r = 0; r < n; ++r)
+        for (int64_t i = 0; i < M; ++i)
+            store(dtype, y[r], i, load(dtype, x, i));
+    return OR_OK;
+}
+
 /* Reduce selected global indices only.  xs[s] holds the K operands of rank s
  * at indices idx[0..K-1] (gathered by the caller; an index >= M takes the
  * identity whatever xs holds there); out receives the K results. */

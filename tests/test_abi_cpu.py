@@ -53,8 +53,9 @@ def header_functions():
 def test_header_declares_the_entry_points():
     names = header_functions()
     assert names == sorted(["vc_shard_count", "vc_reduce_scatter", "vc_all_gather",
-                            "vc_all_reduce", "vc_all_reduce_decomposed",
-                            "vc_all_reduce_decomposed_noalloc", "vc_status_string"])
+                            "vc_all_reduce", "vc_all_reduce_decomposed", "vc_reduce",
+                            "vc_broadcast", "vc_all_reduce_decomposed_noalloc",
+                            "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -255,3 +256,33 @@ def test_noalloc_checks(vc):
     r2[1] = s[2]
     assert na(s, r2, 4, 100) == ALIAS
     assert na(s, list(s), 4, 100) == CUDA  # valid, in place: the launch hook fires
+
+
+def test_reduce_and_broadcast_checks(vc):
+    """Reduce writes one output that may be exactly one input (in place at
+    the root); Broadcast's outputs may include the source itself."""
+    import ctypes
+    L = vc.lib()
+    s, r = fake(4, 1 << 40), fake(4, 2 << 40)
+
+    def red(send, out, n=4, M=100, order=RING):
+        return L.vc_reduce(table(vc, send), ctypes.c_void_p(out), n, M, F32, SUM, order, None)
+
+    def bc(src, outs, n=4, M=100):
+        return L.vc_broadcast(ctypes.c_void_p(src), table(vc, outs), n, M, F32, None)
+
+    assert red(s, r[0]) == CUDA          # valid: the launch hook fires
+    assert red(s, s[2]) == CUDA          # in place at the root
+    assert red(s, s[2] + 8) == ALIAS     # partial overlap
+    assert red(s, 0) == INVALID
+    assert red(s, r[0], order=RH, n=3) == UNSUPPORTED
+    assert red(s, r[0], M=0) == SUCCESS
+    assert bc(s[0], r) == CUDA
+    assert bc(s[0], [s[0]] + r[1:]) == CUDA   # root's own buffer included
+    r2 = list(r)
+    r2[3] = r2[1] + 4
+    assert bc(s[0], r2) == ALIAS
+    r2 = list(r)
+    r2[1] = s[0] + 4
+    assert bc(s[0], r2) == ALIAS
+    assert bc(0, r) == INVALID

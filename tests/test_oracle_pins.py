@@ -536,3 +536,30 @@ def test_bf16_accumulates_in_fp32_and_rounds_once(order):
         y32 = oracle.all_reduce(wide, "float32", op, order)[0]
         ref = torch.from_numpy(y32).to(torch.bfloat16).view(torch.int16).numpy()
         np.testing.assert_array_equal(y16.view(np.int16), ref)
+
+
+# --------------------------------------------------------- reduce / broadcast --
+
+@pytest.mark.parametrize("order", ALL_ORDERS)
+def test_reduce_broadcast_compose_to_allreduce(order):
+    """all_reduce = reduce + broadcast ("通信与互联（01）" 二.2), bit for bit in
+    the same order; the worked example reduces to 600 + 4i at the root."""
+    xs = lin(4, 20)
+    y = oracle.reduce(xs, "int64", "sum", order)
+    np.testing.assert_array_equal(y, 600 + 4 * np.arange(20))
+    for ys in oracle.broadcast(y, 4, "int64"):
+        np.testing.assert_array_equal(ys, y)
+    n, M = 8, 3001
+    xf = si.generate("float32", "uniform_pm1", n, M, seed=17)
+    for op in OPS:
+        ar = oracle.all_reduce(xf, "float32", op, order)
+        out = oracle.broadcast(oracle.reduce(xf, "float32", op, order), n, "float32")
+        for a, b in zip(ar, out):
+            np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_broadcast_is_a_copy():
+    """Every rank receives the root's buffer unchanged (bf16 bits included)."""
+    x = si.generate("bfloat16", "normal", 1, 777, seed=4, sigma=3.0)[0]
+    for y in oracle.broadcast(x, 5, "bfloat16"):
+        np.testing.assert_array_equal(y, x)

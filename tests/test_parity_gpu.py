@@ -520,3 +520,50 @@ def test_user_stream(env):
     s.synchronize()
     oy = oracle.all_reduce(xs, "float32", "sum", "ring")
     assert_bits_equal(to_host(y[0], "float32"), oy[0], "float32", "stream")
+
+
+# -------------------------------------------------------- reduce / broadcast --
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+def test_reduce_and_broadcast(env, dtype):
+    """Reduce = the oracle's reduce (the AllReduce value at the root), bit for
+    bit; Broadcast copies the root's buffer to every output; Reduce then
+    Broadcast equals the fused AllReduce ("通信与互联（01）" 二.2)."""
+    vc, torch = env.vc, env.torch
+    for n, M, op, order in ((4, 20, "sum", "ring"), (8, 1_000_003, "max", "recursive_halving"),
+                            (3, 4099, "prod", "ring"), (64, 5003, "sum", "pairwise_tree"),
+                            (16, 65_537, "avg", "ring"), (1, 333, "min", "ring")):
+        if op == "prod" and dtype in ("float32", "bfloat16"):
+            xs = gen_prod_floats(dtype, n, M)
+        else:
+            xs = gen(dtype, n, M, seed=n + M)
+        for off in (0, 1):
+            d = to_device(torch, xs, dtype, env.dev, offset=off)
+            root = Guarded(env, 1, M, dtype, off)
+            vc.vc_reduce(d, root.views[0], op=op, order=order)
+            outs = Guarded(env, n, M, dtype, off)
+            vc.vc_broadcast(root.views[0], outs.views)
+            ar = [torch.empty_like(t) for t in d]
+            vc.vc_all_reduce(d, ar, op=op, order=order)
+            torch.cuda.synchronize()
+            root.check_guards(env)
+            outs.check_guards(env)
+            want = oracle.reduce(xs, dtype, op, order)
+            got = to_host(root.views[0], dtype)
+            assert_bits_equal(got, want, dtype, f"reduce N={n} M={M} {op} {order} off={off}")
+            for r in range(n):
+                assert_bits_equal(to_host(outs.views[r], dtype), want, dtype, "broadcast")
+                assert torch.equal(ar[r], outs.views[r])
+
+
+def test_reduce_in_place_at_root_and_broadcast_including_root(env):
+    vc, torch = env.vc, env.torch
+    n, M = 8, 100_003
+    xs = gen("float32", n, M, seed=9)
+    d = to_device(torch, xs, "float32", env.dev)
+    want = oracle.reduce(xs, "float32", "sum", "ring")
+    vc.vc_reduce(d, d[3])  # root 3 reduces into its own input
+    vc.vc_broadcast(d[3], d)  # every rank, the root's own buffer included
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_bits_equal(to_host(d[r], "float32"), want, "float32", f"rank {r}")
