@@ -21,7 +21,7 @@ LIB_PATH = _PKG / "_lib" / "libvc.so"
 
 DTYPES = {"int32": 0, "int64": 1, "float32": 2, "bfloat16": 3}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
-ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2}
+ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2, "double_binary_tree": 3}
 STATUS = {0: "VC_SUCCESS", 1: "VC_ERR_INVALID_ARGUMENT", 2: "VC_ERR_UNSUPPORTED",
           3: "VC_ERR_ALIAS", 4: "VC_ERR_CUDA"}
 MAX_RANKS = 64

@@ -31,7 +31,9 @@ int elem_size(vc_dtype_t dt) {
 }
 
 bool valid_op(vc_op_t op) { return op >= VC_SUM && op <= VC_AVG; }
-bool valid_order(vc_order_t o) { return o >= VC_ORDER_RING && o <= VC_ORDER_PAIRWISE_TREE; }
+bool valid_order(vc_order_t o) {
+    return o >= VC_ORDER_RING && o <= VC_ORDER_DOUBLE_BINARY_TREE;
+}
 bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
 // Common checks of every call.  *bytes_m and *bytes_q receive the byte sizes
@@ -115,6 +117,7 @@ vc_status_t launch_reduce(const void* const* in, void* const* out, int n, size_t
     p.M = M;
     p.q = q;
     p.limit = rs ? (long long)n * q : M;
+    p.half = (M + 1) / 2;
     p.inv_q = 1.0f / (float)q;
     p.n = n;
     p.avg = (op == VC_AVG);

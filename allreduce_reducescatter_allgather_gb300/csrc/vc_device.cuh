@@ -25,7 +25,7 @@ constexpr int kRingGroup = 8;  // the same for the ring with a run-time N (whose
                                // run-time rank indices cost more registers)
 constexpr int kWaves = 64;  // grid = up to 64 blocks per SM: many more than resident
 
-enum { kOrderRing = 0, kOrderRecursiveHalving = 1, kOrderPairwiseTree = 2 };
+enum { kOrderRing = 0, kOrderRecursiveHalving = 1, kOrderPairwiseTree = 2, kOrderDoubleTree = 3 };
 
 // Kernel parameters of ReduceScatter / AllReduce.  Passed by value as a
 // __grid_constant__ argument, so the pointer tables live in the parameter
@@ -36,6 +36,7 @@ struct ReduceParams {
     long long M;      // logical elements per rank
     long long q;      // shard length ceil(M / N)
     long long limit;  // index space: N*q for ReduceScatter, M for AllReduce
+    long long half;   // double binary tree: elements below ceil(M/2) use tree A
     float inv_q;      // 1/q, for the chunk estimate
     int n;            // ranks
     int nout;         // outputs the AllReduce kernel writes: n (AllReduce) or 1 (Reduce)
@@ -301,6 +302,17 @@ template <class T, int NR, int U> struct PreLoader {
 
 template <class L> using VecOf = Vec<typename L::A, L::W>;
 
+// The second tree of a double binary tree: node k is played by rank
+// (k + 1) mod N, so every rank index stays a compile-time constant.
+template <class L, int N> struct ShiftedByOne {
+    using A = typename L::A;
+    static constexpr int W = L::W;
+    using Raw = typename L::Raw;
+    const L& l;
+    __device__ __forceinline__ Raw raw(int k) const { return l.raw((k + 1) % N); }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
+};
+
 // --------------------------------------------------------------- orders --
 
 // Ring: chunk c is started by rank c and every later rank on the ring adds
@@ -459,13 +471,19 @@ __device__ __forceinline__ VecOf<L> ring_switch(const L& ld, int c) {
 
 // NT > 0: N is a compile-time constant; NT == 0: ring with a run-time N.
 // The ring switches among its rotations up to N = 8 and folds in groups
-// with run-time rank indices beyond.
+// with run-time rank indices beyond.  `sel` is the ring's chunk, or for the
+// double binary tree which tree (0 = A, 1 = B) the element belongs to.
 template <class Op, int ORDER, int NT, class L>
-__device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int c) {
+__device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int sel) {
+    const int c = sel;
     if constexpr (ORDER == kOrderRecursiveHalving) {
         return rh_group<Op, 0, 1, NT>(ld);
     } else if constexpr (ORDER == kOrderPairwiseTree) {
         return fold_tree<Op, NT>(ld);
+    } else if constexpr (ORDER == kOrderDoubleTree) {
+        if (sel == 0) return fold_tree<Op, NT>(ld);
+        ShiftedByOne<L, NT> shifted{ld};
+        return fold_tree<Op, NT>(shifted);
     } else if constexpr (NT > 0 && NT <= 8) {
         return ring_switch<Op, NT, 0>(ld, c);
     } else {
@@ -526,7 +544,8 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     using A = typename Traits<T>::Acc;
     const int c = chunk_of(i, p.q, p.inv_q, p.n);
     ScalarLoader<T, Op> ld{p, i};
-    Vec<A, 1> v = fold<Op, ORDER, NT>(ld, p.n, c);
+    const int sel = (ORDER == kOrderDoubleTree) ? (i >= p.half) : c;
+    Vec<A, 1> v = fold<Op, ORDER, NT>(ld, p.n, sel);
     A r = v.x[0];
     if (p.avg) r = avg_div(r, p.n);
     if constexpr (RS) {
@@ -543,9 +562,11 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
     constexpr int V = Traits<T>::V;
     const long long i0 = v * V;
     const int c = chunk_of(i0, p.q, p.inv_q, p.n);
-    if (p.vec_ok && i0 + V <= p.M && i0 + V <= (long long)(c + 1) * p.q) {
+    const bool one_tree = (ORDER != kOrderDoubleTree) || i0 >= p.half || i0 + V <= p.half;
+    if (p.vec_ok && one_tree && i0 + V <= p.M && i0 + V <= (long long)(c + 1) * p.q) {
         VecLoader<T> ld{p, i0};
-        auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+        const int sel = (ORDER == kOrderDoubleTree) ? (i0 >= p.half) : c;
+        auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
         store_result<T, NT, RS>(p, c, i0, acc);
     } else {
         for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
@@ -589,7 +610,11 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
             c = chunk_of(v0 * V, p.q, p.inv_q, p.n);
             const long long end = vlast * V + V;
             wide = end <= p.M && end <= (long long)(c + 1) * p.q;
+            if constexpr (ORDER == kOrderDoubleTree)
+                wide = wide && (v0 * V >= p.half || end <= p.half);
         }
+        // the fold's selector: the ring's chunk, or the double tree's half
+        const int sel = (ORDER == kOrderDoubleTree) ? (int)(v0 * V >= p.half) : c;
         if (wide) {
             if constexpr (kPre) {
                 uint4 buf[NT][U];
@@ -602,7 +627,7 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     PreLoader<T, NT, U> ld{buf, u};
-                    auto acc = fold<Op, ORDER, NT>(ld, NT, c);
+                    auto acc = fold<Op, ORDER, NT>(ld, NT, sel);
                     store_result<T, NT, RS>(p, c, (v0 + (long long)u * blockDim.x) * V, acc);
                 }
             } else if constexpr (kTable) {
@@ -629,7 +654,7 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
             } else {
                 static_assert(U == 1, "streaming folds take one vector per thread");
                 VecLoader<T> ld{p, v0 * V};
-                auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+                auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
                 store_result<T, NT, RS>(p, c, v0 * V, acc);
             }
         } else {

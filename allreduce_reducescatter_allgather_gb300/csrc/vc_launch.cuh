@@ -24,7 +24,7 @@ cudaError_t launch_one(const ReduceParams& p, bool rs, cudaStream_t st) {
 // operands at a time.
 template <int N> constexpr int slots_for() { return N <= 4 ? 4 : (N <= 8 ? 2 : 1); }
 
-// Recursive halving and the tree: N = 2, 4, ..., 64.
+// Recursive halving and the (double) tree: N = 2, 4, ..., 64.
 template <class T, class Op, int ORDER>
 cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
     switch (p.n) {
@@ -65,6 +65,7 @@ cudaError_t launch_order(const ReduceParams& p, int order, bool rs, cudaStream_t
     if (p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
     if (order == kOrderRecursiveHalving)
         return launch_pow2<T, Op, kOrderRecursiveHalving>(p, rs, st);
+    if (order == kOrderDoubleTree) return launch_pow2<T, Op, kOrderDoubleTree>(p, rs, st);
     return launch_pow2<T, Op, kOrderPairwiseTree>(p, rs, st);
 }
 

@@ -73,7 +73,7 @@ extern "C" vc_status_t vc_all_reduce_decomposed_noalloc(const void* const* sendb
     if (nranks < 1 || nranks > VC_MAX_RANKS) return VC_ERR_INVALID_ARGUMENT;
     const int es = esize(dtype);
     if (es == 0 || op < VC_SUM || op > VC_AVG) return VC_ERR_INVALID_ARGUMENT;
-    if (order < VC_ORDER_RING || order > VC_ORDER_PAIRWISE_TREE) return VC_ERR_INVALID_ARGUMENT;
+    if (order < VC_ORDER_RING || order > VC_ORDER_DOUBLE_BINARY_TREE) return VC_ERR_INVALID_ARGUMENT;
     if (order != VC_ORDER_RING && (nranks & (nranks - 1)) != 0) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     // the shards must fit the fixed scratch: N shards of q elements, each
@@ -119,6 +119,7 @@ extern "C" vc_status_t vc_all_reduce_decomposed_noalloc(const void* const* sendb
     rp.M = gp.M = (long long)count;
     rp.q = gp.q = (long long)q;
     rp.limit = (long long)nranks * (long long)q;
+    rp.half = ((long long)count + 1) / 2;
     rp.inv_q = gp.inv_q = 1.0f / (float)q;
     rp.n = gp.n = nranks;
     rp.nout = nranks;

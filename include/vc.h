@@ -93,11 +93,17 @@ typedef enum {
  *    with the single child N/2; rank r's level is its lowest set bit L and its
  *    parent is (r-L) | 2L; odd ranks are leaves).  An inner node's value is
  *    (left subtree (+) right subtree) (+) its own operand, the lower-ranked
- *    child on the left.  N must be a power of two. */
+ *    child on the left.  N must be a power of two.
+ *  DOUBLE_BINARY_TREE: two complementary trees, each carrying half of the
+ *    data ("通信与互联（01）" 六.3): the first ceil(count/2) elements in the
+ *    PAIRWISE_TREE order (tree A), the others in tree B, which is tree A with
+ *    every rank number shifted by one (node k is rank (k+1) mod N: root rank
+ *    1, its child rank N/2 + 1, ...).  N must be a power of two. */
 typedef enum {
     VC_ORDER_RING = 0,
     VC_ORDER_RECURSIVE_HALVING = 1,
-    VC_ORDER_PAIRWISE_TREE = 2
+    VC_ORDER_PAIRWISE_TREE = 2,
+    VC_ORDER_DOUBLE_BINARY_TREE = 3
 } vc_order_t;
 
 typedef enum {
@@ -106,7 +112,7 @@ typedef enum {
      * size, nranks outside [1, VC_MAX_RANKS], an unknown enum value, or a
      * count whose byte size exceeds 2^62 */
     VC_ERR_INVALID_ARGUMENT = 1,
-    /* RECURSIVE_HALVING or PAIRWISE_TREE with nranks not a power of two */
+    /* RECURSIVE_HALVING or a tree order with nranks not a power of two */
     VC_ERR_UNSUPPORTED = 2,
     /* an output range overlaps an input range or another output range (the
      * only overlap allowed is the in-place AllReduce, recvbufs[r] ==

@@ -27,7 +27,8 @@ _LIB = _HERE / "liboracle.so"
 # Enumerations of the oracle (its own numbering; mapped from names below).
 DTYPES = {"int32": 0, "int64": 1, "float32": 2, "bfloat16": 3}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
-ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2, "sequential": 3}
+ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2, "sequential": 3,
+          "double_binary_tree": 4}
 
 # numpy storage type of each dtype (bfloat16 is carried as its raw uint16 bits)
 NP_STORAGE = {"int32": np.int32, "int64": np.int64, "float32": np.float32,

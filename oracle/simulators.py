@@ -238,3 +238,27 @@ def tree_reduce_broadcast(bufs, op: str = "sum"):
         have |= {r for r in range(n) if parents[r] in have}
         bcast_rounds += 1
     return [result.copy() for _ in range(n)], parents, reduce_rounds + bcast_rounds
+
+
+def tree_b_parent(r: int, n: int) -> int:
+    """Parent of rank r in the second tree of a double binary tree: the
+    first tree with every rank number shifted by one (even n)."""
+    p = tree_parent((r - 1) % n, n)
+    return -1 if p == -1 else (p + 1) % n
+
+
+def double_tree_reduce_broadcast(bufs, op: str = "sum"):
+    """Each rank's buffer is cut in two halves (the first ceil(M/2)
+    elements, the rest); the first half is reduced and broadcast over the
+    tree, the second over the shifted tree.  Returns (outputs, parents of
+    tree B)."""
+    n = len(bufs)
+    M = np.asarray(bufs[0]).size
+    h = (M + 1) // 2
+    first = [np.asarray(b)[:h] for b in bufs]
+    # tree B: node k of the plain tree is played by rank (k+1) mod n
+    second = [np.asarray(bufs[(k + 1) % n])[h:] for k in range(n)]
+    out_a, _, _ = tree_reduce_broadcast(first, op)
+    out_b, _, _ = tree_reduce_broadcast(second, op)
+    outs = [np.concatenate([out_a[r], out_b[r]]) for r in range(n)]
+    return outs, [tree_b_parent(r, n) for r in range(n)]

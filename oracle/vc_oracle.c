@@ -31,6 +31,8 @@
  *  - tree: "通信与互联（01）" 六.1 figure: rank 0 is the root with one child,
  *    a rank's level is the lowest set bit of its number, odd ranks are leaves;
  *    an inner node receives both children, adds itself, sends to its parent.
+ *  - double binary tree: same page, 六.3: two trees, the second the first with
+ *    every rank number shifted by one; each carries half of the data.
  *
  * Readings where the pages are silent (each one is also listed in the design
  * notes):
@@ -45,7 +47,9 @@
  *  - tree inner node: (left subtree (+) right subtree) (+) own value, the
  *    lower-numbered child on the left (parity unpinned: the pages fix only
  *    the tree's shape);
- *  - recursive halving and tree are defined for N a power of two only.
+ *  - recursive halving and tree are defined for N a power of two only;
+ *  - double binary tree: tree A reduces the first ceil(M/2) elements of the
+ *    buffer, tree B (ranks shifted by one) the rest, padding included.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math).
  */
@@ -57,7 +61,7 @@
 enum { OR_INT32 = 0, OR_INT64 = 1, OR_FLOAT32 = 2, OR_BFLOAT16 = 3 };
 enum { OR_SUM = 0, OR_PROD = 1, OR_MAX = 2, OR_MIN = 3, OR_AVG = 4 };
 enum { OR_RING = 0, OR_RECURSIVE_HALVING = 1, OR_PAIRWISE_TREE = 2,
-       OR_SEQUENTIAL = 3 };
+       OR_SEQUENTIAL = 3, OR_DOUBLE_TREE = 4 };
 
 enum { OR_OK = 0, OR_BAD_ARGUMENT = -1, OR_UNSUPPORTED = -2, OR_NO_MEMORY = -3 };
 
@@ -340,9 +344,10 @@ static int plan_init(plan_t *pl, int n, int64_t M, int dtype, int op, int order)
         return OR_BAD_ARGUMENT;
     if (op < OR_SUM || op > OR_AVG)
         return OR_BAD_ARGUMENT;
-    if (order < OR_RING || order > OR_SEQUENTIAL)
+    if (order < OR_RING || order > OR_DOUBLE_TREE)
         return OR_BAD_ARGUMENT;
-    if ((order == OR_RECURSIVE_HALVING || order == OR_PAIRWISE_TREE) && !is_pow2(n))
+    if ((order == OR_RECURSIVE_HALVING || order == OR_PAIRWISE_TREE ||
+         order == OR_DOUBLE_TREE) && !is_pow2(n))
         return OR_UNSUPPORTED;
     pl->n = n;
     pl->M = M;
@@ -350,7 +355,7 @@ static int plan_init(plan_t *pl, int n, int64_t M, int dtype, int op, int order)
     pl->dtype = dtype;
     pl->op = op;
     pl->order = order;
-    if (order == OR_PAIRWISE_TREE)
+    if (order == OR_PAIRWISE_TREE || order == OR_DOUBLE_TREE)
         tree_build(&pl->tree, n);
     return OR_OK;
 }
@@ -364,6 +369,17 @@ static val_t reduce_operands(const plan_t *pl, const val_t *a, int64_t i)
     case OR_RING: v = fold_ring(pl->op, a, pl->n, c); break;
     case OR_RECURSIVE_HALVING: v = fold_recursive_halving(pl->op, a, pl->n, c); break;
     case OR_PAIRWISE_TREE: v = fold_tree_node(pl->op, a, &pl->tree, 0); break;
+    case OR_DOUBLE_TREE:
+        if (i < (pl->M + 1) / 2) {
+            v = fold_tree_node(pl->op, a, &pl->tree, 0); /* tree A */
+        } else {
+            /* tree B: the same tree with node k played by rank (k+1) mod N */
+            val_t b[OR_MAX_RANKS];
+            for (int k = 0; k < pl->n; ++k)
+                b[k] = a[(k + 1) % pl->n];
+            v = fold_tree_node(pl->op, b, &pl->tree, 0);
+        }
+        break;
     default: v = fold_sequential(pl->op, a, pl->n); break;
     }
     return epilogue(pl->op, pl->n, v);

@@ -17,7 +17,7 @@ from conftest import ROOT
 SUCCESS, INVALID, UNSUPPORTED, ALIAS, CUDA = 0, 1, 2, 3, 4
 I32, I64, F32, BF16 = 0, 1, 2, 3
 SUM, PROD, MAX, MIN, AVG = 0, 1, 2, 3, 4
-RING, RH, TREE = 0, 1, 2
+RING, RH, TREE, DTREE = 0, 1, 2, 3
 MiB = 1 << 20
 
 
@@ -117,7 +117,7 @@ def test_unknown_enums(vc):
     s, r = fake(4, 1 << 40), fake(4, 2 << 40)
     assert rs(vc, s, r, 4, 100, dt=9) == INVALID
     assert rs(vc, s, r, 4, 100, op=5) == INVALID
-    assert rs(vc, s, r, 4, 100, order=3) == INVALID
+    assert rs(vc, s, r, 4, 100, order=4) == INVALID
     assert ar(vc, s, r, 4, 100, dt=-1) == INVALID
     assert ag(vc, s, r, 4, 100, dt=7) == INVALID
 
@@ -145,11 +145,13 @@ def test_power_of_two_orders(vc):
         s, r = fake(n, 1 << 40), fake(n, 2 << 40)
         assert rs(vc, s, r, n, 1000, order=RH) == UNSUPPORTED
         assert ar(vc, s, r, n, 1000, order=TREE) == UNSUPPORTED
+        assert ar(vc, s, r, n, 1000, order=DTREE) == UNSUPPORTED
         assert ar(vc, s, r, n, 1000, order=RING) == CUDA
     for n in (1, 2, 4, 8, 16, 32, 64):
         s, r = fake(n, 1 << 40), fake(n, 2 << 40)
         assert ar(vc, s, r, n, 1000, order=RH) == CUDA
         assert rs(vc, s, r, n, 1000, order=TREE) == CUDA
+        assert rs(vc, s, r, n, 1000, order=DTREE) == CUDA
 
 
 def test_alias_rules(vc):

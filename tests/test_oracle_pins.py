@@ -19,7 +19,7 @@ from oracle import simulators as sim
 import synthetic_inputs as si
 from conftest import ints, read_golden
 
-ORDERS = ["ring", "recursive_halving", "pairwise_tree"]
+ORDERS = ["ring", "recursive_halving", "pairwise_tree", "double_binary_tree"]
 ALL_ORDERS = ORDERS + ["sequential"]
 OPS = ["sum", "prod", "max", "min", "avg"]
 
@@ -175,6 +175,10 @@ def test_hand_derived_fp32_orders():
     for order in ("recursive_halving", "pairwise_tree", "sequential"):
         y = oracle.all_reduce(xs, "float32", "sum", order)[0]
         assert all(_bits(v) == int(g[order], 0) for v in y), order
+    # double binary tree: elements 0, 1 (first half) tree A, 2, 3 tree B
+    y = oracle.all_reduce(xs, "float32", "sum", "double_binary_tree")[0]
+    assert [_bits(v) for v in y] == [int(g["pairwise_tree"], 0)] * 2 + \
+        [int(g["double_tree_b"], 0)] * 2
 
 
 def test_ring_schedule_tables_n4():
@@ -563,3 +567,38 @@ def test_broadcast_is_a_copy():
     x = si.generate("bfloat16", "normal", 1, 777, seed=4, sigma=3.0)[0]
     for y in oracle.broadcast(x, 5, "bfloat16"):
         np.testing.assert_array_equal(y, x)
+
+
+# ------------------------------------------------------- double binary tree --
+
+def test_double_tree_shape_n8():
+    """Tree B of the figure: root r1 -> r5 -> {r3, r7}, r3 -> {r2, r4},
+    r7 -> {r6, r0}; A's inner nodes are B's leaves and the reverse."""
+    g = read_golden("double_tree_n8.txt")
+    pb = [sim.tree_b_parent(r, 8) for r in range(8)]
+    assert pb == ints(g["parents_b"])
+    leaves_b = [r for r in range(8) if r not in pb]
+    inner_b = sorted(set(p for p in pb if p >= 0) | {pb.index(-1)})
+    assert leaves_b == ints(g["leaves_b"]) and inner_b == ints(g["inner_b"])
+    pa = list(oracle.tree_parents(8))
+    inner_a = sorted(set(p for p in pa if p >= 0))
+    assert inner_a == leaves_b
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 64])
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
+def test_double_tree_replay_equals_oracle(n, op):
+    """Halves reduced over the tree and the shifted tree, replayed, equal the
+    oracle's double_binary_tree fold bit for bit (odd M: the first half is
+    the larger)."""
+    M = 4 * n + 3
+    xs = si.generate("float32", "uniform_pm1", n, M, seed=70 + n)
+    if op == "prod":
+        xs = [np.float32(1.0) + x * np.float32(0.25) for x in xs]
+    outs, _ = sim.double_tree_reduce_broadcast(xs, op)
+    y = oracle.all_reduce(xs, "float32", op, "double_binary_tree")
+    for o, yy in zip(outs, y):
+        np.testing.assert_array_equal(o.view(np.uint32), yy.view(np.uint32))
+    h = (M + 1) // 2
+    tree = oracle.all_reduce(xs, "float32", op, "pairwise_tree")[0]
+    np.testing.assert_array_equal(y[0][:h].view(np.uint32), tree[:h].view(np.uint32))

@@ -23,7 +23,7 @@ from gpu_util import assert_bits_equal, bits, to_device, to_host, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
-ORDERS = ["ring", "recursive_halving", "pairwise_tree"]
+ORDERS = ["ring", "recursive_halving", "pairwise_tree", "double_binary_tree"]
 OPS = ["sum", "prod", "max", "min", "avg"]
 GUARD = 32  # guard elements after every output buffer
 
@@ -198,7 +198,7 @@ def test_max_is_not_zero_padded(env):
 
 # ------------------------------------------------------ workload configs --
 
-@pytest.mark.parametrize("order", ["ring", "recursive_halving", "pairwise_tree"])
+@pytest.mark.parametrize("order", ORDERS)
 @pytest.mark.parametrize("op", OPS)
 def test_n8_m1000003_fp32(env, op, order):
     """Eight ranks, 1,000,003 fp32 uniform[-1,1) (q = 125,001, five padding
@@ -346,7 +346,7 @@ def _sweep_cases(max_bytes):
                 if nbytes > max_bytes or n * nbytes > (64 << 30):
                     continue
                 op = SWEEP_OPS[k % 4]
-                order = ORDERS[(k // 4) % 3]
+                order = ORDERS[(k // 4) % 4]
                 k += 1
                 cases.append((dtype, n, nbytes // es, op, order))
     return cases
