@@ -28,7 +28,7 @@ MAX_RANKS = 64
 
 # Every function the header declares (checked by the tests against vc.h).
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
-           "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast",
+           "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles",
            "vc_all_reduce_decomposed_noalloc", "vc_status_string")
 
 
@@ -62,8 +62,9 @@ def lib() -> ctypes.CDLL:
         L.vc_all_reduce_decomposed.argtypes = [vpp, vpp, vpp, i32, sz, i32, i32, i32, vp]
         L.vc_reduce.argtypes = [vpp, vp, i32, sz, i32, i32, i32, vp]
         L.vc_broadcast.argtypes = [vp, vpp, i32, sz, i32, vp]
+        L.vc_copy_tiles.argtypes = [vp, i32, vp]
         for f in ("vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
-                  "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast"):
+                  "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles"):
             getattr(L, f).restype = i32
         L.vc_status_string.argtypes = [i32]
         L.vc_status_string.restype = ctypes.c_char_p

@@ -20,7 +20,7 @@ BUILD = PKG / "_build"
 LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "libvc.so"
 
-SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu"]
+SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu", "vc_copy.cu"]
 HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
 # vc_reduce_inst.cu compiled once per (element type, op): (object, -D flags)
 INSTANCE_SOURCE = "vc_reduce_inst.cu"

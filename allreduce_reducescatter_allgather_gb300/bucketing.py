@@ -1,0 +1,162 @@
+"""Gradient buckets for the virtual-rank AllReduce.
+
+What the pages say ("Ring AllReduce 核心流程" 4; "通信与互联（01）" 三.1 and
+九.1): small tensors are merged into buckets before the collective, so one
+large message replaces many small ones.  DDP fills a bucket while backward
+runs and sends it when it is full.  Its caps are 25 MiB per bucket
+(kDefaultBucketBytesCap), and 1 MiB for the first bucket
+(kDefaultFirstBucketBytes) so that something can be sent early.  On one GPU the
+saving is one kernel launch per bucket instead of one per tensor, and a
+bucket large enough to run at the HBM rate.
+
+Two ways to feed a bucket:
+ - views (no copy): every gradient tensor is a view into its rank's flat
+   bucket buffer (what DDP calls gradients as bucket views); the AllReduce
+   runs in place on the buckets and the views hold the results;
+ - packing: tensors that live elsewhere are copied into the buckets and back
+   with vc_copy_tiles, one launch per direction per bucket.
+
+Assignment rule (the pages give only the caps; this is the plain reading):
+tensors are taken in reverse order, the order backward produces their
+gradients.  A bucket closes when the next tensor would take it past its cap.
+The first bucket's cap is the small one.  A tensor larger than the cap gets a
+bucket of its own.  Inside a bucket every tensor starts on a 16-byte boundary.
+Padding elements are zero and are reduced like the rest (zero in, identity
+out for SUM; never read back).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from . import _binding
+
+FIRST_BUCKET_BYTES = 1 << 20  # kDefaultFirstBucketBytes
+BUCKET_BYTES = 25 << 20       # kDefaultBucketBytesCap
+ALIGN_BYTES = 16
+TILE_BYTES = 1 << 16          # VC_COPY_TILE_MAX_BYTES
+
+
+def assign_buckets(nbytes, first_cap: int = FIRST_BUCKET_BYTES, cap: int = BUCKET_BYTES):
+    """Bucket membership for tensors of the given sizes (bytes, in forward
+    order): a list of buckets, each a list of tensor indices in the order
+    they are filled (reverse tensor order)."""
+    buckets, cur, size = [], [], 0
+    limit = first_cap
+    for t in reversed(range(len(nbytes))):
+        b = int(nbytes[t])
+        if cur and size + b > limit:
+            buckets.append(cur)
+            cur, size = [], 0
+            limit = cap
+        cur.append(t)
+        size += b
+    if cur:
+        buckets.append(cur)
+    return buckets
+
+
+@dataclass
+class _Bucket:
+    tensors: list      # tensor indices in the bucket, in fill order
+    offsets: list      # element offset of each of them in the bucket buffer
+    count: int         # elements in the bucket buffer (padding included)
+    buffers: list      # one flat device buffer per rank
+    pack_tiles: object = None    # device table for vc_copy_tiles (tensors -> bucket)
+    unpack_tiles: object = None  # (bucket -> tensors)
+    ntiles: int = 0
+
+
+class GradientBuckets:
+    """Flat bucket buffers for `nranks` virtual ranks, each holding tensors
+    of the given shapes (the same on every rank) and dtype."""
+
+    def __init__(self, shapes, dtype, nranks: int, device, first_cap: int = FIRST_BUCKET_BYTES,
+                 cap: int = BUCKET_BYTES):
+        import torch
+        self.torch = torch
+        self.shapes = [tuple(s) for s in shapes]
+        self.numels = [int(torch.Size(s).numel()) for s in self.shapes]
+        self.dtype = dtype
+        self.nranks = nranks
+        self.device = torch.device(device)
+        es = torch.empty(0, dtype=dtype).element_size()
+        self.es = es
+        align = ALIGN_BYTES // es
+        self.buckets = []
+        self.where = [None] * len(self.shapes)  # tensor -> (bucket, offset)
+        for members in assign_buckets([n * es for n in self.numels], first_cap, cap):
+            offsets, off = [], 0
+            for t in members:
+                off = (off + align - 1) // align * align
+                offsets.append(off)
+                off += self.numels[t]
+            count = max(1, (off + align - 1) // align * align)
+            bufs = [torch.zeros(count, dtype=dtype, device=self.device) for _ in range(nranks)]
+            b = _Bucket(members, offsets, count, bufs)
+            for t, o in zip(members, offsets):
+                self.where[t] = (len(self.buckets), o)
+            self.buckets.append(b)
+
+    # ---------------------------------------------------------- views --
+    def views(self, rank: int):
+        """Tensors of `rank` as views into its bucket buffers (forward order):
+        write gradients into them, then call all_reduce()."""
+        out = []
+        for t, shape in enumerate(self.shapes):
+            bi, off = self.where[t]
+            buf = self.buckets[bi].buffers[rank]
+            out.append(buf[off:off + self.numels[t]].view(shape))
+        return out
+
+    def all_reduce(self, op: str = "sum", order: str = "ring", stream=None):
+        """One in-place AllReduce per bucket."""
+        for b in self.buckets:
+            _binding.vc_all_reduce(b.buffers, None, op=op, order=order, stream=stream)
+
+    # -------------------------------------------------------- packing --
+    def _tiles(self, b: _Bucket, grads, to_bucket: bool):
+        rows = []
+        for r in range(self.nranks):
+            base = b.buffers[r].data_ptr()
+            for t, off in zip(b.tensors, b.offsets):
+                g = grads[r][t]
+                nbytes = self.numels[t] * self.es
+                tp, bp = g.data_ptr(), base + off * self.es
+                for k in range(0, nbytes, TILE_BYTES):
+                    n = min(TILE_BYTES, nbytes - k)
+                    rows.append((tp + k, bp + k, n) if to_bucket else (bp + k, tp + k, n))
+        return rows
+
+    def bind(self, grads):
+        """Build the pack / unpack tables for grads[rank][tensor] (tensors
+        outside the buckets, contiguous, of the given shapes and dtype).  The
+        tables hold the tensors' addresses: rebind if the tensors change."""
+        torch = self.torch
+        for r in range(self.nranks):
+            for t, g in enumerate(grads[r]):
+                if not (g.is_cuda and g.is_contiguous() and g.dtype == self.dtype
+                        and g.numel() == self.numels[t] and g.device == self.device):
+                    raise ValueError(f"grads[{r}][{t}] does not match the bucket layout")
+        for b in self.buckets:
+            pack = self._tiles(b, grads, True)
+            unpack = self._tiles(b, grads, False)
+            b.pack_tiles = torch.tensor(pack, dtype=torch.int64).to(self.device)
+            b.unpack_tiles = torch.tensor(unpack, dtype=torch.int64).to(self.device)
+            b.ntiles = len(pack)
+        self.bound = grads
+
+    def all_reduce_tensors(self, op: str = "sum", order: str = "ring", stream=None):
+        """For the bound tensors: per bucket, pack (one launch), AllReduce in
+        place (one launch), unpack (one launch)."""
+        torch = self.torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        import ctypes
+        L = _binding.lib()
+        s = ctypes.c_void_p(stream.cuda_stream)
+        for b in self.buckets:
+            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
+                                                  b.ntiles, s))
+            _binding.vc_all_reduce(b.buffers, None, op=op, order=order, stream=stream)
+            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.unpack_tiles.data_ptr()),
+                                                  b.ntiles, s))

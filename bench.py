@@ -361,6 +361,7 @@ def run_ours(args, workload: dict):
                 "algorithmic_bytes_per_launch": by["fused_ar"]}
 
     memory = memory_report(torch, vc, d, args, dev) if not args.no_memory else None
+    buckets = bucket_report(torch, vc, args, dev) if not args.no_memory else None
     e2e = e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, by["step"])
 
     line = {
@@ -379,6 +380,8 @@ def run_ours(args, workload: dict):
                           "reasons": clk["reasons"], "samples": clk["samples"]}
     if memory is not None:
         line["memory_mib"] = memory
+    if buckets is not None:
+        line["gradient_buckets"] = buckets
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         g, steps, secs = time_oracle(workload, args.op, args.order, args.cpu_seconds,
                                      window=1 << 22)
@@ -507,6 +510,71 @@ def memory_report(torch, vc, d, args, dev):
     return out
 
 
+def transformer_grad_shapes(layers: int = 12, hidden: int = 1024, vocab: int = 32000):
+    """Gradient shapes of a small synthetic transformer (forward order):
+    token embedding, then per layer two layer norms and four linear layers
+    with biases."""
+    h = hidden
+    shapes = [(vocab, h)]
+    for _ in range(layers):
+        shapes += [(h,), (h,), (3 * h, h), (3 * h,), (h, h), (h,),
+                   (h,), (h,), (4 * h, h), (4 * h,), (h, 4 * h), (h,)]
+    return shapes
+
+
+def bucket_report(torch, vc, args, dev):
+    """One AllReduce per gradient tensor against one per 25 MiB bucket (the
+    pages' DDP buckets), on 8 virtual ranks of bf16 gradients: with the
+    gradients as bucket views (no copy) and with packing."""
+    from allreduce_reducescatter_allgather_gb300 import bucketing
+    n = 8
+    shapes = transformer_grad_shapes()
+    gb = bucketing.GradientBuckets(shapes, torch.bfloat16, n, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(99)
+    grads = [[torch.randn(s, generator=g, device=dev).to(torch.bfloat16) for s in shapes]
+             for _ in range(n)]
+    gb.bind(grads)
+    total = sum(t.numel() for t in grads[0]) * 2
+    stream = torch.cuda.current_stream(dev)
+
+    def per_tensor():
+        for t in range(len(shapes)):
+            vc.vc_all_reduce([grads[r][t] for r in range(n)], None, op=args.op,
+                             order=args.order, stream=stream)
+
+    def views():
+        gb.all_reduce(op=args.op, order=args.order, stream=stream)
+
+    def packed():
+        gb.all_reduce_tensors(op=args.op, order=args.order, stream=stream)
+
+    def t_ms(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    ar_bytes = 2 * n * total
+    out = {"ranks": n, "dtype": "bf16", "tensors": len(shapes), "buckets": len(gb.buckets),
+           "bytes_per_rank": total}
+    for name, fn, launches in (("per_tensor", per_tensor, len(shapes)),
+                               ("bucket_views", views, len(gb.buckets)),
+                               ("bucket_packed", packed, 3 * len(gb.buckets))):
+        ms = t_ms(fn)
+        out[name] = {"us": round(ms * 1e3, 1), "allreduce_gbs": round(ar_bytes / ms / 1e6, 1),
+                     "launches": launches}
+    del grads, gb
+    torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     import synthetic_inputs as si
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -523,7 +591,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-memory", action="store_true")
+    ap.add_argument("--no-memory", action="store_true",
+                    help="skip the memory-lifetime and gradient-bucket reports")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

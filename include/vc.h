@@ -192,6 +192,30 @@ vc_status_t vc_reduce(const void *const *sendbufs, void *recvbuf, int nranks, si
 vc_status_t vc_broadcast(const void *sendbuf, void *const *recvbufs, int nranks, size_t count,
                          vc_dtype_t dtype, vc_stream_t stream);
 
+/* One byte range to copy: `bytes` bytes from src to dst (device memory). */
+typedef struct {
+    const void *src;
+    void *dst;
+    size_t bytes;
+} vc_copy_tile_t;
+
+/* The largest tile vc_copy_tiles takes; longer ranges are split by the
+ * caller into several tiles. */
+#define VC_COPY_TILE_MAX_BYTES (1u << 16)
+
+/* Copies many independent byte ranges in one launch: the packing of many
+ * small tensors into a bucket buffer before its AllReduce, and the unpacking
+ * after it (the pages' DDP buckets: gradients are merged into 25 MiB buckets,
+ * the first one 1 MiB, so one large collective replaces many small ones --
+ * "通信与互联（01）" 三.1 and 九.1; "Ring AllReduce 核心流程" 4).
+ * dev_tiles: a DEVICE array of ntiles entries (8-byte aligned), each with
+ * 0 < bytes <= VC_COPY_TILE_MAX_BYTES, src and dst device pointers.  The
+ * entries live in device memory, so the library cannot check them: ranges
+ * that are invalid, overlap each other's destinations, or overlap within a
+ * tile are undefined behaviour, as for any device copy.  ntiles == 0
+ * launches nothing. */
+vc_status_t vc_copy_tiles(const vc_copy_tile_t *dev_tiles, int ntiles, vc_stream_t stream);
+
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
  * 32 MiB on every GPU that loads this library, held until the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)

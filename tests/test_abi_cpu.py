@@ -54,8 +54,8 @@ def test_header_declares_the_entry_points():
     names = header_functions()
     assert names == sorted(["vc_shard_count", "vc_reduce_scatter", "vc_all_gather",
                             "vc_all_reduce", "vc_all_reduce_decomposed", "vc_reduce",
-                            "vc_broadcast", "vc_all_reduce_decomposed_noalloc",
-                            "vc_status_string"])
+                            "vc_broadcast", "vc_copy_tiles",
+                            "vc_all_reduce_decomposed_noalloc", "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -288,3 +288,13 @@ def test_reduce_and_broadcast_checks(vc):
     r2[1] = s[0] + 4
     assert bc(s[0], r2) == ALIAS
     assert bc(0, r) == INVALID
+
+
+def test_copy_tiles_checks(vc):
+    import ctypes
+    L = vc.lib()
+    assert L.vc_copy_tiles(None, 0, None) == SUCCESS
+    assert L.vc_copy_tiles(None, 3, None) == INVALID
+    assert L.vc_copy_tiles(ctypes.c_void_p(1 << 40), -1, None) == INVALID
+    assert L.vc_copy_tiles(ctypes.c_void_p((1 << 40) + 4), 3, None) == INVALID
+    assert L.vc_copy_tiles(ctypes.c_void_p(1 << 40), 3, None) == CUDA  # launch hook

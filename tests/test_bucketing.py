@@ -1,0 +1,145 @@
+"""Gradient buckets: DDP's assignment rule with the pages' caps (CPU), and the
+bucketed AllReduce on the GPU against the oracle run on the same bucket
+layout."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from conftest import ints, read_golden
+from gpu_util import assert_bits_equal, to_host
+
+MiB = 1 << 20
+
+
+def test_assignment_matches_hand_derivation():
+    from allreduce_reducescatter_allgather_gb300.bucketing import (
+        BUCKET_BYTES, FIRST_BUCKET_BYTES, assign_buckets)
+    assert FIRST_BUCKET_BYTES == 1 * MiB and BUCKET_BYTES == 25 * MiB
+    g = read_golden("ddp_buckets.txt")
+    sizes = [int(float(s) * MiB) for s in g["sizes_mib"].split()]
+    got = assign_buckets(sizes)
+    want = [ints(g[f"bucket{k}"]) for k in range(4)]
+    assert got == want
+
+
+def test_assignment_invariants():
+    from allreduce_reducescatter_allgather_gb300.bucketing import assign_buckets
+    rng = np.random.default_rng(0)
+    sizes = [int(x) for x in rng.integers(1, 8 * MiB, 300)]
+    buckets = assign_buckets(sizes)
+    flat = [t for b in buckets for t in b]
+    assert flat == list(reversed(range(len(sizes))))  # every tensor once, backward order
+    for k, b in enumerate(buckets):
+        cap = 1 * MiB if k == 0 else 25 * MiB
+        total = sum(sizes[t] for t in b)
+        assert total <= cap or len(b) == 1
+        if k + 1 < len(buckets):  # closed because the next tensor did not fit
+            assert total + sizes[buckets[k + 1][0]] > cap
+
+
+# ------------------------------------------------------------------ GPU --
+
+SHAPES = [(3,), (17, 5), (1000,), (256, 256), (4099,), (64, 1024), (7, 7, 7), (300_001,),
+          (2,), (1 << 20,), (12345,), (513, 9), (1,)]
+
+
+@pytest.fixture(scope="module")
+def genv():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import allreduce_reducescatter_allgather_gb300 as vc
+    from allreduce_reducescatter_allgather_gb300 import bucketing
+    dev = torch.device("cuda:0")
+    return torch, vc, bucketing, dev
+
+
+def _oracle_buckets(gb, grads_np, dtype, op, order):
+    """The oracle's AllReduce of every bucket, laid out as the library lays
+    it out (zero padding included), sliced back into tensors."""
+    out = [[None] * len(gb.shapes) for _ in range(gb.nranks)]
+    st = oracle.NP_STORAGE[dtype]
+    for b in gb.buckets:
+        bufs = [np.zeros(b.count, st) for _ in range(gb.nranks)]
+        for r in range(gb.nranks):
+            for t, off in zip(b.tensors, b.offsets):
+                bufs[r][off:off + gb.numels[t]] = grads_np[r][t]
+        ys = oracle.all_reduce(bufs, dtype, op, order)
+        for r in range(gb.nranks):
+            for t, off in zip(b.tensors, b.offsets):
+                out[r][t] = ys[r][off:off + gb.numels[t]]
+    return out
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,op,order", [("float32", "sum", "ring"),
+                                            ("bfloat16", "avg", "recursive_halving"),
+                                            ("int64", "max", "double_binary_tree")])
+def test_bucket_views_and_packing_match_oracle(genv, dtype, op, order):
+    torch, vc, bk, dev = genv
+    n = 8
+    tdt = {"float32": torch.float32, "bfloat16": torch.bfloat16, "int64": torch.int64}[dtype]
+    dist = "uniform_int" if dtype == "int64" else "uniform_pm1"
+    kw = {"lo": -100, "hi": 100} if dtype == "int64" else {}
+    # small caps so that this set spans several buckets
+    gb = bk.GradientBuckets(SHAPES, tdt, n, dev, first_cap=64 << 10, cap=2 * MiB)
+    assert len(gb.buckets) >= 3
+    grads_np = [[si.generate_rank(dtype, dist, 11 + t, r, gb.numels[t], **kw)
+                 for t in range(len(SHAPES))] for r in range(n)]
+    want = _oracle_buckets(gb, grads_np, dtype, op, order)
+
+    def to_dev(a):
+        if dtype == "bfloat16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    # views: write the gradients into the bucket views, reduce in place
+    for r in range(n):
+        for t, v in enumerate(gb.views(r)):
+            v.copy_(to_dev(grads_np[r][t]).view(v.shape))
+    gb.all_reduce(op=op, order=order)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t, v in enumerate(gb.views(r)):
+            assert_bits_equal(to_host(v.reshape(-1), dtype), want[r][t], dtype, f"view r{r} t{t}")
+    # packing: separately allocated tensors, packed, reduced, unpacked
+    for b in gb.buckets:
+        for buf in b.buffers:
+            buf.zero_()
+    grads = [[to_dev(grads_np[r][t]).view(SHAPES[t]).clone() for t in range(len(SHAPES))]
+             for r in range(n)]
+    gb.bind(grads)
+    gb.all_reduce_tensors(op=op, order=order)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t in range(len(SHAPES)):
+            assert_bits_equal(to_host(grads[r][t].reshape(-1), dtype), want[r][t], dtype,
+                              f"packed r{r} t{t}")
+
+
+@pytest.mark.gpu
+def test_bucketed_equals_per_tensor_for_chunk_free_orders(genv):
+    """Recursive halving and the tree fold every element the same way
+    wherever it sits, so bucketed and per-tensor AllReduce agree bit for bit
+    (the ring's rotation depends on the element's chunk, so it does not)."""
+    torch, vc, bk, dev = genv
+    n = 4
+    gb = bk.GradientBuckets(SHAPES, torch.float32, n, dev)
+    src = [[torch.randn(s, device=dev) for s in SHAPES] for _ in range(n)]
+    grads = [[g.clone() for g in row] for row in src]
+    gb.bind(grads)
+    for order in ("recursive_halving", "pairwise_tree"):
+        for r in range(n):
+            for t in range(len(SHAPES)):
+                grads[r][t].copy_(src[r][t])
+        gb.all_reduce_tensors(order=order)
+        for t in range(len(SHAPES)):
+            ref = [torch.empty_like(src[0][t]) for _ in range(n)]
+            vc.vc_all_reduce([src[r][t] for r in range(n)], ref, order=order)
+            for r in range(n):
+                assert torch.equal(grads[r][t], ref[r])
