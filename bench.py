@@ -168,11 +168,27 @@ def aggregate(torch, local_ms: float, local_bytes: int, world: int):
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_window_step(xs, dtype, op, order):
-    """One oracle step over host windows: fused AR then decomposed AR."""
-    import oracle
-    oracle.all_reduce(xs, dtype, op, order)
-    oracle.all_reduce_decomposed(xs, dtype, op, order)
+class OracleStep:
+    """One oracle step over host windows: fused AR then decomposed AR, into
+    output arrays allocated once (so the timing is the oracle's arithmetic,
+    not the host's page faults)."""
+
+    def __init__(self, xs, dtype, op, order):
+        import numpy as np
+        import oracle
+        self.oracle, self.xs, self.dtype, self.op, self.order = oracle, xs, dtype, op, order
+        n, M = len(xs), xs[0].size
+        st = oracle.NP_STORAGE[dtype]
+        q = oracle.shard_count(M, n)
+        self.y = [np.zeros(M, st) for _ in range(n)]
+        self.y2 = [np.zeros(M, st) for _ in range(n)]
+        self.z = [np.zeros(q, st) for _ in range(n)]
+
+    def __call__(self):
+        o = self.oracle
+        o.all_reduce(self.xs, self.dtype, self.op, self.order, out=self.y)
+        o.all_reduce_decomposed(self.xs, self.dtype, self.op, self.order, shards=self.z,
+                                out=self.y2)
 
 
 def host_window(workload: dict, window: int):
@@ -190,9 +206,11 @@ def time_oracle(workload: dict, op: str, order: str, seconds: float, window: int
     n, dtype = workload["n"], workload["dtype"]
     W = xs[0].size
     b = step_bytes(n, W, ESIZE[dtype])["step"]
+    step = OracleStep(xs, dtype, op, order)
+    step()
     steps, t0 = 0, time.perf_counter()
     while True:
-        oracle_window_step(xs, dtype, op, order)
+        step()
         steps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -207,22 +225,25 @@ def run_reference(args, workload: dict):
     import oracle
     oracle.build()
     n, dtype = workload["n"], workload["dtype"]
-    # size the window so that warmup + steps take about a minute
-    calib = host_window(workload, 1 << 16)
+    # size the window so that warmup + steps take about a minute: time two
+    # steps on a 2^18-element window (outputs preallocated, as in the run)
+    calib = OracleStep(host_window(workload, 1 << 18), dtype, args.op, args.order)
+    calib()
     t0 = time.perf_counter()
-    oracle_window_step(calib, dtype, args.op, args.order)
-    per_elem = (time.perf_counter() - t0) / calib[0].size
+    calib()
+    calib()
+    per_elem = (time.perf_counter() - t0) / 2 / calib.xs[0].size
     budget = 60.0 / max(1, args.steps + args.warmup)
     window = 1 << 12
     while window * 2 * per_elem <= budget and window * 2 <= workload["M"]:
         window *= 2
-    xs = host_window(workload, window)
-    W = xs[0].size
+    step = OracleStep(host_window(workload, window), dtype, args.op, args.order)
+    W = step.xs[0].size
     for _ in range(args.warmup):
-        oracle_window_step(xs, dtype, args.op, args.order)
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_window_step(xs, dtype, args.op, args.order)
+        step()
     el = time.perf_counter() - t0
     b = step_bytes(n, W, ESIZE[dtype])["step"]
     value = b * args.steps / el / 1e9

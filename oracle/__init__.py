@@ -140,23 +140,35 @@ def all_gather(zs, M: int, dtype: str):
     return ys
 
 
-def all_reduce(xs, dtype: str, op: str, order: str):
-    """y[r][i] = reduction over s of x[s][i], identical for every r."""
+def _outputs(out, n, count, dtype):
+    """Caller-supplied output arrays (checked), or new ones."""
+    if out is None:
+        return [np.empty(count, NP_STORAGE[dtype]) for _ in range(n)]
+    if len(out) != n or any(o.dtype != NP_STORAGE[dtype] or o.size != count
+                            or not o.flags.c_contiguous for o in out):
+        raise TypeError("output arrays do not match")
+    return out
+
+
+def all_reduce(xs, dtype: str, op: str, order: str, out=None):
+    """y[r][i] = reduction over s of x[s][i], identical for every r.  `out`:
+    optional preallocated outputs (N arrays of M)."""
     xs = _as_inputs(xs, dtype)
     n, M = len(xs), xs[0].size
-    ys = [np.empty(M, NP_STORAGE[dtype]) for _ in range(n)]
+    ys = _outputs(out, n, M, dtype)
     _check(lib().oracle_all_reduce(_ptrs(xs), _ptrs(ys), n, M, DTYPES[dtype], OPS[op],
                                    ORDERS[order]))
     return ys
 
 
-def all_reduce_decomposed(xs, dtype: str, op: str, order: str):
-    """ReduceScatter into N shards of q, then AllGather; returns (shards, outputs)."""
+def all_reduce_decomposed(xs, dtype: str, op: str, order: str, shards=None, out=None):
+    """ReduceScatter into N shards of q, then AllGather; returns (shards,
+    outputs).  `shards`, `out`: optional preallocated arrays."""
     xs = _as_inputs(xs, dtype)
     n, M = len(xs), xs[0].size
     q = shard_count(M, n)
-    zs = [np.empty(q, NP_STORAGE[dtype]) for _ in range(n)]
-    ys = [np.empty(M, NP_STORAGE[dtype]) for _ in range(n)]
+    zs = _outputs(shards, n, q, dtype)
+    ys = _outputs(out, n, M, dtype)
     _check(lib().oracle_all_reduce_decomposed(_ptrs(xs), _ptrs(zs), _ptrs(ys), n, M,
                                               DTYPES[dtype], OPS[op], ORDERS[order]))
     return zs, ys
