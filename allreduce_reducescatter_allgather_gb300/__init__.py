@@ -12,7 +12,12 @@ from ._binding import (  # noqa: F401
     OPS,
     ORDERS,
     VcError,
+    Prepared,
     lib,
+    prepare_all_gather,
+    prepare_all_reduce,
+    prepare_all_reduce_decomposed,
+    prepare_reduce_scatter,
     vc_all_gather,
     vc_all_reduce,
     vc_all_reduce_decomposed,

@@ -91,13 +91,19 @@ def _torch():
     return torch
 
 
+_DTYPE_NAMES = None
+
+
 def _dtype_name(t) -> str:
-    torch = _torch()
-    names = {torch.int32: "int32", torch.int64: "int64", torch.float32: "float32",
-             torch.bfloat16: "bfloat16"}
-    if t.dtype not in names:
+    global _DTYPE_NAMES
+    if _DTYPE_NAMES is None:
+        torch = _torch()
+        _DTYPE_NAMES = {torch.int32: "int32", torch.int64: "int64", torch.float32: "float32",
+                        torch.bfloat16: "bfloat16"}
+    name = _DTYPE_NAMES.get(t.dtype)
+    if name is None:
         raise TypeError(f"unsupported dtype {t.dtype}; use int32, int64, float32 or bfloat16")
-    return names[t.dtype]
+    return name
 
 
 def _check_tensors(name: str, ts, dtype: str, numel: int, device):
@@ -231,6 +237,82 @@ def vc_broadcast(sendbuf, recvbufs, stream=None):
     _check_tensors("recvbufs", recvbufs, dt, M, dev)
     check_status(lib().vc_broadcast(ctypes.c_void_p(sendbuf.data_ptr()), _ptrs(recvbufs), n, M,
                                     DTYPES[dt], _stream(stream, dev)))
+
+
+# ------------------------------------------------------ prepared calls --
+
+class Prepared:
+    """A collective on fixed buffers, checked once: every call is then one
+    C call (the library still repeats its own pointer checks).  Holds
+    references to its tensors, so they stay alive as long as the handle.
+
+        ar = prepare_all_reduce(sendbufs, recvbufs, op="sum", order="ring")
+        ar()                 # on the current stream
+        ar(stream=s)         # on another torch stream
+    """
+
+    def __init__(self, fn, args, tensors, device):
+        self._fn = fn
+        self._args = args
+        self._tensors = tensors
+        self._device = device
+
+    def __call__(self, stream=None):
+        check_status(self._fn(*self._args, _stream(stream, self._device)))
+
+
+def prepare_all_reduce(sendbufs, recvbufs=None, op: str = "sum", order: str = "ring"):
+    """vc_all_reduce on these buffers (recvbufs=None: in place)."""
+    n = len(sendbufs)
+    recvbufs = list(sendbufs) if recvbufs is None else list(recvbufs)
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    args = (_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order])
+    return Prepared(lib().vc_all_reduce, args, (list(sendbufs), recvbufs), dev)
+
+
+def prepare_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum",
+                                  order: str = "ring"):
+    """vc_all_reduce_decomposed on these buffers (recvbufs=None: in place)."""
+    n = len(sendbufs)
+    recvbufs = list(sendbufs) if recvbufs is None else list(recvbufs)
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    _check_tensors("shardbufs", shardbufs, dt, vc_shard_count(M, n), dev)
+    args = (_ptrs(sendbufs), _ptrs(shardbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
+            ORDERS[order])
+    return Prepared(lib().vc_all_reduce_decomposed, args,
+                    (list(sendbufs), list(shardbufs), recvbufs), dev)
+
+
+def prepare_reduce_scatter(sendbufs, recvbufs, op: str = "sum", order: str = "ring"):
+    """vc_reduce_scatter on these buffers."""
+    n = len(sendbufs)
+    dt = _dtype_name(sendbufs[0])
+    M = sendbufs[0].numel()
+    dev = sendbufs[0].device
+    _check_tensors("sendbufs", sendbufs, dt, M, dev)
+    _check_tensors("recvbufs", recvbufs, dt, vc_shard_count(M, n), dev)
+    args = (_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order])
+    return Prepared(lib().vc_reduce_scatter, args, (list(sendbufs), list(recvbufs)), dev)
+
+
+def prepare_all_gather(sendbufs, recvbufs):
+    """vc_all_gather on these buffers."""
+    n = len(sendbufs)
+    dt = _dtype_name(recvbufs[0])
+    M = recvbufs[0].numel()
+    dev = recvbufs[0].device
+    _check_tensors("recvbufs", recvbufs, dt, M, dev)
+    _check_tensors("sendbufs", sendbufs, dt, vc_shard_count(M, n), dev)
+    args = (_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt])
+    return Prepared(lib().vc_all_gather, args, (list(sendbufs), list(recvbufs)), dev)
 
 
 # ------------------------------------------------ no-allocation variant --

@@ -83,6 +83,7 @@ class GradientBuckets:
         self.es = es
         align = ALIGN_BYTES // es
         self.buckets = []
+        self._prepared = {}
         self.where = [None] * len(self.shapes)  # tensor -> (bucket, offset)
         for members in assign_buckets([n * es for n in self.numels], first_cap, cap):
             offsets, off = [], 0
@@ -108,10 +109,21 @@ class GradientBuckets:
             out.append(buf[off:off + self.numels[t]].view(shape))
         return out
 
+    def _calls(self, op: str, order: str):
+        """The buckets' in-place AllReduce calls, prepared once per op and
+        order (a call is then one C call per bucket)."""
+        key = (op, order)
+        calls = self._prepared.get(key)
+        if calls is None:
+            calls = [_binding.prepare_all_reduce(b.buffers, None, op=op, order=order)
+                     for b in self.buckets]
+            self._prepared[key] = calls
+        return calls
+
     def all_reduce(self, op: str = "sum", order: str = "ring", stream=None):
         """One in-place AllReduce per bucket."""
-        for b in self.buckets:
-            _binding.vc_all_reduce(b.buffers, None, op=op, order=order, stream=stream)
+        for c in self._calls(op, order):
+            c(stream=stream)
 
     # -------------------------------------------------------- packing --
     def _tiles(self, b: _Bucket, grads, to_bucket: bool):
@@ -154,9 +166,9 @@ class GradientBuckets:
         import ctypes
         L = _binding.lib()
         s = ctypes.c_void_p(stream.cuda_stream)
-        for b in self.buckets:
+        for b, c in zip(self.buckets, self._calls(op, order)):
             _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
                                                   b.ntiles, s))
-            _binding.vc_all_reduce(b.buffers, None, op=op, order=order, stream=stream)
+            c(stream=stream)
             _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.unpack_tiles.data_ptr()),
                                                   b.ntiles, s))

@@ -383,6 +383,7 @@ def run_ours(args, workload: dict):
 
     memory = memory_report(torch, vc, d, args, dev) if not args.no_memory else None
     buckets = bucket_report(torch, vc, args, dev) if not args.no_memory else None
+    latency = latency_table(torch, vc, args, dev) if not args.no_memory else None
     e2e = e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, by["step"])
 
     line = {
@@ -403,6 +404,8 @@ def run_ours(args, workload: dict):
         line["memory_mib"] = memory
     if buckets is not None:
         line["gradient_buckets"] = buckets
+    if latency is not None:
+        line["direct_vs_decomposed"] = latency
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         g, steps, secs = time_oracle(workload, args.op, args.order, args.cpu_seconds,
                                      window=1 << 22)
@@ -565,6 +568,78 @@ def memory_report(torch, vc, d, args, dev):
     return out
 
 
+def latency_table(torch, vc, args, dev):
+    """p1's direct-vs-decomposed experiment on four virtual ranks ("NCCL 专家
+    课程 07", 性能实验为什么交替执行顺序 / 严格处理不稳定点): per-rank sizes 1 KiB,
+    64 KiB, 1 MiB, 16 MiB, 256 MiB of fp32; 3 warm-ups, then 10 cycles that
+    alternate which path runs first; inputs reset and synchronised outside
+    each timed call; median / P95 / CV of the per-call CUDA-event times; the
+    decomposed / direct ratio is given only when both CVs are at most 5 %."""
+    import numpy as np
+    n = 4
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for nbytes in (1 << 10, 64 << 10, 1 << 20, 16 << 20, 256 << 20):
+        M = nbytes // 4
+        g = torch.Generator(device=dev)
+        g.manual_seed(nbytes)
+        base = [torch.randn(M, generator=g, device=dev) for _ in range(n)]
+        work = [t.clone() for t in base]
+        shards = [torch.empty(vc.vc_shard_count(M, n), device=dev) for _ in range(n)]
+
+        def reset():
+            for w, b in zip(work, base):
+                w.copy_(b)
+            torch.cuda.synchronize()
+
+        # prepared calls: checked once, one C call each (the first C call on
+        # the stream, as a user with persistent buffers would issue it)
+        ar = vc.prepare_all_reduce(work, None, op=args.op, order=args.order)
+        dec = vc.prepare_all_reduce_decomposed(work, shards, None, op=args.op,
+                                               order=args.order)
+
+        def direct():
+            ar(stream=stream)
+
+        def decomposed():
+            dec(stream=stream)
+
+        def timed(fn):
+            reset()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) * 1e3  # µs
+
+        for _ in range(3):
+            timed(direct)
+            timed(decomposed)
+        t = {"direct": [], "decomposed": []}
+        for cycle in range(10):
+            order = ("direct", "decomposed") if cycle % 2 == 0 else ("decomposed", "direct")
+            for mode in order:
+                t[mode].append(timed(direct if mode == "direct" else decomposed))
+        row = {"bytes_per_rank": nbytes}
+        for mode, v in t.items():
+            a = np.array(v)
+            med = float(np.median(a))
+            row[mode] = {"median_us": round(med, 3), "p95_us": round(float(np.percentile(a, 95)), 3),
+                         "cv": round(float(a.std() / a.mean()), 4),
+                         "payload_gbs": round(nbytes * n / med / 1e3, 2),
+                         "hbm_gbs": round(step_bytes(n, M, 4)["fused_ar" if mode == "direct"
+                                                               else "decomposed_ar"] / med / 1e3, 1)}
+        stable = row["direct"]["cv"] <= 0.05 and row["decomposed"]["cv"] <= 0.05
+        row["decomposed_over_direct"] = (round(row["decomposed"]["median_us"]
+                                               / row["direct"]["median_us"], 3)
+                                         if stable else "unstable")
+        rows.append(row)
+        del base, work, shards, ar, dec
+    torch.cuda.empty_cache()
+    return rows
+
+
 def transformer_grad_shapes(layers: int = 12, hidden: int = 1024, vocab: int = 32000):
     """Gradient shapes of a small synthetic transformer (forward order):
     token embedding, then per layer two layer norms and four linear layers
@@ -593,10 +668,12 @@ def bucket_report(torch, vc, args, dev):
     total = sum(t.numel() for t in grads[0]) * 2
     stream = torch.cuda.current_stream(dev)
 
+    singles = [vc.prepare_all_reduce([grads[r][t] for r in range(n)], None, op=args.op,
+                                     order=args.order) for t in range(len(shapes))]
+
     def per_tensor():
-        for t in range(len(shapes)):
-            vc.vc_all_reduce([grads[r][t] for r in range(n)], None, op=args.op,
-                             order=args.order, stream=stream)
+        for c in singles:
+            c(stream=stream)
 
     def views():
         gb.all_reduce(op=args.op, order=args.order, stream=stream)
@@ -625,7 +702,7 @@ def bucket_report(torch, vc, args, dev):
         ms = t_ms(fn)
         out[name] = {"us": round(ms * 1e3, 1), "allreduce_gbs": round(ar_bytes / ms / 1e6, 1),
                      "launches": launches}
-    del grads, gb
+    del grads, gb, singles
     torch.cuda.empty_cache()
     return out
 
@@ -647,7 +724,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-memory", action="store_true",
-                    help="skip the memory-lifetime and gradient-bucket reports")
+                    help="skip the memory-lifetime, gradient-bucket and latency reports")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

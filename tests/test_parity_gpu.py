@@ -567,3 +567,32 @@ def test_reduce_in_place_at_root_and_broadcast_including_root(env):
     torch.cuda.synchronize()
     for r in range(n):
         assert_bits_equal(to_host(d[r], "float32"), want, "float32", f"rank {r}")
+
+
+def test_prepared_calls_match_direct_calls(env):
+    """Prepared handles (checked once, one C call per use) give the same bits
+    as the direct calls, on the current stream and on another one."""
+    vc, torch = env.vc, env.torch
+    n, M = 8, 300_007
+    xs = gen("float32", n, M, seed=21)
+    d = to_device(torch, xs, "float32", env.dev)
+    q = vc.vc_shard_count(M, n)
+    y, y2 = [torch.empty_like(t) for t in d], [torch.empty_like(t) for t in d]
+    z = [torch.empty(q, device=env.dev) for _ in range(n)]
+    g = [torch.empty_like(t) for t in d]
+    for order in ORDERS:
+        vc.prepare_all_reduce(d, y, order=order)()
+        vc.prepare_reduce_scatter(d, z, order=order)()
+        vc.prepare_all_gather(z, g)()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        vc.prepare_all_reduce_decomposed(d, [torch.empty_like(t) for t in z], y2,
+                                         order=order)(stream=s)
+        torch.cuda.synchronize()
+        oy = oracle.all_reduce(xs, "float32", "sum", order)
+        oz = oracle.reduce_scatter(xs, "float32", "sum", order)
+        for r in range(n):
+            assert_bits_equal(to_host(y[r], "float32"), oy[r], "float32", "prepared AR")
+            assert_bits_equal(to_host(y2[r], "float32"), oy[r], "float32", "prepared dec")
+            assert_bits_equal(to_host(g[r], "float32"), oy[r], "float32", "prepared AG")
+            assert_bits_equal(to_host(z[r], "float32"), oz[r], "float32", "prepared RS")
