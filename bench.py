@@ -720,7 +720,7 @@ def main(argv=None):
                     choices=["ring", "recursive_halving", "pairwise_tree"])
     ap.add_argument("--elements", type=int, default=0,
                     help="override the elements per rank (small cases for profiling)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-memory", action="store_true",
