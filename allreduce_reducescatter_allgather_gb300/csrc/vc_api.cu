@@ -179,38 +179,50 @@ vc_status_t launch_broadcast(const void* src, void* const* out, int nout, size_t
 
 }  // namespace
 
-// Grid size for the grid-stride kernels: one block per kThreads units, at
-// most kWaves blocks per SM (the SM count is queried once per device).
-int grid_blocks(long long units) {
+// SMs of the current device, queried once per device; -1 on error.
+int sm_count() {
     static std::mutex mu;
-    static int sm_count[VC_MAX_RANKS] = {0};
+    static int count[VC_MAX_RANKS] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= VC_MAX_RANKS) return -1;
-    int sms = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (sm_count[dev] == 0) {
-            int v = 0;
-            if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                return -1;
-            sm_count[dev] = v;
-        }
-        sms = sm_count[dev];
+    std::lock_guard<std::mutex> lock(mu);
+    if (count[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        count[dev] = v;
     }
+    return count[dev];
+}
+
+// Grid size for the grid-stride kernels: one block per kThreads units, at
+// most kWaves blocks per SM.
+int grid_blocks(long long units) {
+    const int sms = sm_count();
+    if (sms < 1) return -1;
     const long long want = (units + kThreads - 1) / kThreads;
     const long long cap = (long long)sms * kWaves;
     const long long b = want < cap ? want : cap;
     return (int)(b < 1 ? 1 : b);
 }
 
-cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st) {
+cudaError_t launch_gather(const GatherParams& p_in, int esize, cudaStream_t st) {
+    GatherParams p = p_in;
     const long long nvec = (p.M * esize + 15) / 16;
     const int blocks = grid_blocks((nvec + kGatherSlots - 1) / kGatherSlots);
     if (blocks < 1) return cudaErrorInvalidConfiguration;
+    // Rank groups: double them while the grid is short of ~8 blocks per SM
+    // and every group keeps at least 4 outputs (so the extra source reads stay
+    // a quarter of the writes at most).
+    const int target = 8 * sm_count();  // 8 blocks per SM
+    int groups = 1;
+    while ((long long)blocks * groups < target && p.n / (groups * 2) >= 4) groups *= 2;
+    p.rpg = (p.n + groups - 1) / groups;
+    const dim3 grid(blocks, groups);
     switch (esize) {
-    case 2: vc_ag_kernel<2><<<blocks, kThreads, 0, st>>>(p); break;
-    case 4: vc_ag_kernel<4><<<blocks, kThreads, 0, st>>>(p); break;
-    case 8: vc_ag_kernel<8><<<blocks, kThreads, 0, st>>>(p); break;
+    case 2: vc_ag_kernel<2><<<grid, kThreads, 0, st>>>(p); break;
+    case 4: vc_ag_kernel<4><<<grid, kThreads, 0, st>>>(p); break;
+    case 8: vc_ag_kernel<8><<<grid, kThreads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

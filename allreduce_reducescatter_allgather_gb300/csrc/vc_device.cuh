@@ -53,6 +53,9 @@ struct GatherParams {
     float inv_q;
     int n;       // outputs written (and shards read, for AllGather)
     int vec_ok;  // every output base 16-byte aligned
+    int rpg;     // outputs per rank group: block row y writes outputs
+                 // [y*rpg, min(n, (y+1)*rpg)) (more rows when M alone is too
+                 // small to fill the GPU)
 };
 
 // ---------------------------------------------------------------- types --
@@ -690,6 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1) vc_ar_kernel(const __grid_constan
 // and is written to all N outputs.  It moves bits only, so it is typed by
 // element size alone.  Like the reductions, a thread takes kGatherSlots
 // vectors (blockDim.x apart) and loads all of them before it stores any.
+// When the M output indices alone give too few blocks for the GPU (small M,
+// many ranks), the outputs are split into groups along the grid's y axis:
+// each group re-reads the (small) source and writes its share of the ranks.
 template <int ES> struct Bits;
 template <> struct Bits<2> { using U = unsigned short; };
 template <> struct Bits<4> { using U = unsigned; };
@@ -713,20 +719,20 @@ __device__ __forceinline__ uint4 gather_load(const GatherParams& p, int s, long 
 }
 
 template <int ES>
-__device__ __noinline__ void gather_slot(const GatherParams& p, long long v) {
+__device__ __noinline__ void gather_slot(const GatherParams& p, long long v, int r0, int r1) {
     using U = typename Bits<ES>::U;
     constexpr int V = 16 / ES;
     const long long i0 = v * V;
     const int s = chunk_of(i0, p.q, p.inv_q, p.n);
     if (p.vec_ok && i0 + V <= p.M && i0 + V <= (long long)(s + 1) * p.q) {
         const uint4 val = gather_load<ES>(p, s, i0);
-        for (int r = 0; r < p.n; ++r) st16(static_cast<U*>(p.out[r]) + i0, val);
+        for (int r = r0; r < r1; ++r) st16(static_cast<U*>(p.out[r]) + i0, val);
     } else {
         for (int k = 0; k < V && i0 + k < p.M; ++k) {
             const long long i = i0 + k;
             const int si = chunk_of(i, p.q, p.inv_q, p.n);
             const U val = static_cast<const U*>(p.in[si])[i - (long long)si * p.q];
-            for (int r = 0; r < p.n; ++r) static_cast<U*>(p.out[r])[i] = val;
+            for (int r = r0; r < r1; ++r) static_cast<U*>(p.out[r])[i] = val;
         }
     }
 }
@@ -738,6 +744,8 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
     constexpr int S = kGatherSlots;
     const long long nvec = (p.M + V - 1) / V;
     const long long span = (long long)blockDim.x * S;
+    const int r0 = (int)blockIdx.y * p.rpg;
+    const int r1 = min(p.n, r0 + p.rpg);
     for (long long b0 = (long long)blockIdx.x * span; b0 < nvec; b0 += (long long)gridDim.x * span) {
         const long long v0 = b0 + threadIdx.x;
         const long long vlast = v0 + (long long)(S - 1) * blockDim.x;
@@ -752,7 +760,7 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
             uint4 val[S];
 #pragma unroll
             for (int u = 0; u < S; ++u) val[u] = gather_load<ES>(p, s, (v0 + (long long)u * blockDim.x) * V);
-            for (int r = 0; r < p.n; ++r) {
+            for (int r = r0; r < r1; ++r) {
                 U* dst = static_cast<U*>(p.out[r]) + v0 * V;
 #pragma unroll
                 for (int u = 0; u < S; ++u) st16(dst + (long long)u * blockDim.x * V, val[u]);
@@ -761,7 +769,7 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
 #pragma unroll 1
             for (int u = 0; u < S; ++u) {
                 const long long v = v0 + (long long)u * blockDim.x;
-                if (v < nvec) gather_slot<ES>(p, v);
+                if (v < nvec) gather_slot<ES>(p, v, r0, r1);
             }
         }
     }
@@ -779,5 +787,8 @@ cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st);
 // once keep the blocks in flight on neighbouring addresses, which the HBM
 // serves faster than one resident wave striding over the whole buffer.)
 int grid_blocks(long long units);
+
+// SMs of the current device (queried once per device); -1 on error.
+int sm_count();
 
 }  // namespace vc

@@ -707,6 +707,76 @@ def bucket_report(torch, vc, args, dev):
     return out
 
 
+def run_sweep(args):
+    """The size x rank-count sweep (per-rank bytes 8 KiB * 4^k and 1 GiB, N in
+    {2, 4, 8, 16, 64}, N * bytes <= 64 GiB) over the four element types: one
+    JSON line per point with RS / AG / fused AR GB/s and their fraction of the
+    measured copy peak (SUM, the order given by --order).  Inputs are made on
+    the device; each kernel's time is the median of 5 single calls after 3
+    warm-ups, with the L2 flushed before each call where the data could
+    otherwise stay in it."""
+    import torch
+
+    import allreduce_reducescatter_allgather_gb300 as vc
+    import synthetic_inputs as si
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = measured_peak()
+    stream = torch.cuda.current_stream(dev)
+
+    # a buffer twice the L2: writing it between calls evicts the last call's
+    # data, so points whose data would fit in L2 are still timed from HBM
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+
+    def t_ms(fn, small, reps=5):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            if small:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        return sorted(times)[len(times) // 2]
+
+    for n, nbytes in si.sweep_points():
+        if args.order != "ring" and n & (n - 1):
+            continue
+        for dtype in ("float32", "bfloat16", "int32", "int64"):
+            es = ESIZE[dtype]
+            M = nbytes // es
+            dist = "uniform_pm1" if dtype in ("float32", "bfloat16") else "uniform_int"
+            kw = {} if dist == "uniform_pm1" else {"lo": -100, "hi": 100}
+            d = si.generate_device(torch, dtype, dist, n, M, si.SEED_BASE + 4, dev, **kw)
+            q = vc.vc_shard_count(M, n)
+            z = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+            rs = vc.prepare_reduce_scatter(d, z, op=args.op, order=args.order)
+            ag = vc.prepare_all_gather(z, d)  # AG writes over the inputs, after RS
+            ar = vc.prepare_all_reduce(d, None, op=args.op, order=args.order)  # in place
+            b = step_bytes(n, M, es)
+            small = 2 * n * nbytes < 4 * l2  # inputs + outputs could stay in L2
+            line = {"sweep": "size_x_ranks", "n": n, "bytes_per_rank": nbytes, "dtype": dtype,
+                    "op": args.op, "order": args.order, "peak": peak, "peak_kind": kind,
+                    "timing": "median of 5 single calls" + (", L2 flushed before each"
+                                                            if small else "")}
+            for name, fn, key in (("reduce_scatter", rs, "reduce_scatter"),
+                                  ("all_gather", ag, "all_gather"),
+                                  ("all_reduce", ar, "fused_ar")):
+                ms = t_ms(lambda: fn(stream=stream), small)
+                g = b[key] / (ms / 1e3) / 1e9
+                line[name] = {"us": round(ms * 1e3, 2), "gbs": round(g, 1),
+                              "frac": round(g / peak, 4)}
+            print(json.dumps(line), flush=True)
+            del d, z, rs, ag, ar
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     import synthetic_inputs as si
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -723,6 +793,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the size x rank-count sweep instead (one JSON line per point)")
     ap.add_argument("--no-memory", action="store_true",
                     help="skip the memory-lifetime, gradient-bucket and latency reports")
     args = ap.parse_args(argv)
@@ -733,6 +805,10 @@ def main(argv=None):
         workload["M"] = args.elements
     if args.impl == "reference":
         return run_reference(args, workload)
+    if args.sweep:
+        import __graft_entry__
+        __graft_entry__.build()
+        return run_sweep(args)
     if dist_info()[0] == 1:
         import __graft_entry__
         __graft_entry__.build()  # under torchrun the library must be built beforehand
