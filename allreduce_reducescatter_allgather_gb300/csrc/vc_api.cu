@@ -1,6 +1,7 @@
 // The C ABI of include/vc.h: argument checks on the host, then one launch
 // (two for the decomposed AllReduce) on the caller's stream.  Nothing is
 // allocated; the pointer tables travel by value in the kernel parameters.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -69,17 +70,36 @@ Range range_of(const void* p, size_t bytes) {
 
 // Outputs must be pairwise disjoint and disjoint from every input, except
 // that output r may be exactly input r when allow_in_place is set.
+// O(N log N): the outputs are sorted by start address, so they are disjoint
+// iff each ends before the next starts; an input can then only overlap the
+// first output that ends after the input starts (outputs beyond it start
+// later still), or -- when that one is its own in-place output, which ends
+// exactly where the input ends -- none.
 vc_status_t check_alias(const void* const* in, size_t in_bytes, void* const* out,
                         size_t out_bytes, int n, bool allow_in_place) {
-    for (int r = 0; r < n; ++r) {
-        const Range o = range_of(out[r], out_bytes);
-        for (int s = 0; s < n; ++s) {
-            if (s != r && overlap(o, range_of(out[s], out_bytes))) return VC_ERR_ALIAS;
-            const Range i = range_of(in[s], in_bytes);
-            if (!overlap(o, i)) continue;
-            const bool same = allow_in_place && s == r && in[s] == out[r] && in_bytes == out_bytes;
-            if (!same) return VC_ERR_ALIAS;
+    if (out_bytes == 0) return VC_SUCCESS;
+    int order[VC_MAX_RANKS];
+    for (int r = 0; r < n; ++r) order[r] = r;
+    std::sort(order, order + n, [&](int a, int b) {
+        return reinterpret_cast<uintptr_t>(out[a]) < reinterpret_cast<uintptr_t>(out[b]);
+    });
+    Range sorted[VC_MAX_RANKS];
+    for (int k = 0; k < n; ++k) sorted[k] = range_of(out[order[k]], out_bytes);
+    for (int k = 0; k + 1 < n; ++k)
+        if (sorted[k].hi > sorted[k + 1].lo) return VC_ERR_ALIAS;
+    if (in_bytes == 0) return VC_SUCCESS;
+    for (int s = 0; s < n; ++s) {
+        const Range i = range_of(in[s], in_bytes);
+        // first output whose end lies beyond the input's start
+        int lo = 0, hi = n;
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if (sorted[mid].hi <= i.lo) lo = mid + 1; else hi = mid;
         }
+        if (lo == n || !overlap(sorted[lo], i)) continue;
+        const int r = order[lo];
+        const bool same = allow_in_place && r == s && in[s] == out[r] && in_bytes == out_bytes;
+        if (!same) return VC_ERR_ALIAS;
     }
     return VC_SUCCESS;
 }

@@ -290,8 +290,13 @@ def run_ours(args, workload: dict):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
+        import datetime
+
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+        # a rank that dies or never arrives ends the others' next collective
+        # with an error after this long, instead of leaving them waiting
+        dist.init_process_group("nccl", device_id=dev,
+                                timeout=datetime.timedelta(seconds=args.dist_timeout))
 
     w = dict(workload)
     n, M, dtype = w.pop("n"), w.pop("M"), w.pop("dtype")
@@ -655,7 +660,8 @@ def transformer_grad_shapes(layers: int = 12, hidden: int = 1024, vocab: int = 3
 def bucket_report(torch, vc, args, dev):
     """One AllReduce per gradient tensor against one per 25 MiB bucket (the
     pages' DDP buckets), on 8 virtual ranks of bf16 gradients: with the
-    gradients as bucket views (no copy) and with packing."""
+    gradients as bucket views (no copy) and with packing; the per-tensor and
+    bucket loops also replayed from a CUDA graph (launch cost amortised)."""
     from allreduce_reducescatter_allgather_gb300 import bucketing
     n = 8
     shapes = transformer_grad_shapes()
@@ -671,15 +677,17 @@ def bucket_report(torch, vc, args, dev):
     singles = [vc.prepare_all_reduce([grads[r][t] for r in range(n)], None, op=args.op,
                                      order=args.order) for t in range(len(shapes))]
 
+    # each loop runs on the current stream: the bench's, or the capture
+    # stream while a CUDA graph records it
     def per_tensor():
         for c in singles:
-            c(stream=stream)
+            c()
 
     def views():
-        gb.all_reduce(op=args.op, order=args.order, stream=stream)
+        gb.all_reduce(op=args.op, order=args.order)
 
     def packed():
-        gb.all_reduce_tensors(op=args.op, order=args.order, stream=stream)
+        gb.all_reduce_tensors(op=args.op, order=args.order)
 
     def t_ms(fn, reps=10):
         for _ in range(3):
@@ -693,16 +701,30 @@ def bucket_report(torch, vc, args, dev):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    def graphed(fn):
+        """The loop captured once in a CUDA graph; each call replays it."""
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+        return g.replay
+
+    graphs = []
+
     ar_bytes = 2 * n * total
     out = {"ranks": n, "dtype": "bf16", "tensors": len(shapes), "buckets": len(gb.buckets),
            "bytes_per_rank": total}
     for name, fn, launches in (("per_tensor", per_tensor, len(shapes)),
+                               ("per_tensor_graph", graphed(per_tensor), len(shapes)),
                                ("bucket_views", views, len(gb.buckets)),
+                               ("bucket_views_graph", graphed(views), len(gb.buckets)),
                                ("bucket_packed", packed, 3 * len(gb.buckets))):
         ms = t_ms(fn)
         out[name] = {"us": round(ms * 1e3, 1), "allreduce_gbs": round(ar_bytes / ms / 1e6, 1),
                      "launches": launches}
-    del grads, gb, singles
+    del grads, gb, singles, graphs
     torch.cuda.empty_cache()
     return out
 
@@ -791,6 +813,8 @@ def main(argv=None):
     ap.add_argument("--elements", type=int, default=0,
                     help="override the elements per rank (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--dist-timeout", type=float, default=300.0,
+                    help="seconds a rank waits in a collective for the others (torchrun)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",

@@ -298,3 +298,52 @@ def test_copy_tiles_checks(vc):
     assert L.vc_copy_tiles(ctypes.c_void_p(1 << 40), -1, None) == INVALID
     assert L.vc_copy_tiles(ctypes.c_void_p((1 << 40) + 4), 3, None) == INVALID
     assert L.vc_copy_tiles(ctypes.c_void_p(1 << 40), 3, None) == CUDA  # launch hook
+
+
+def test_alias_check_agrees_with_pairwise_rule(vc):
+    """The O(N log N) overlap check gives the same answer as the plain
+    pairwise rule on random layouts (many overlapping, many disjoint)."""
+    import random
+    rnd = random.Random(7)
+    M, es = 100, 4
+    nb = M * es
+
+    def pairwise(ins, outs, in_place):
+        for r in range(len(outs)):
+            for s in range(len(outs)):
+                o0, o1 = outs[r], outs[r] + nb
+                if s != r and o0 < outs[s] + nb and outs[s] < o1:
+                    return ALIAS
+                if ins[s] < o1 and o0 < ins[s] + nb:
+                    if not (in_place and s == r and ins[s] == outs[r]):
+                        return ALIAS
+        return CUDA  # valid: the launch hook fires
+
+    seen = {ALIAS: 0, CUDA: 0}
+    for trial in range(600):
+        n = rnd.choice([1, 2, 3, 4, 8, 17, 64])
+        base = 1 << 40
+        spread = rnd.choice([2, 40, 400])  # dense layouts collide, sparse ones do not
+        slots = [base + 16 * rnd.randrange(0, spread * n) for _ in range(2 * n)]
+        if spread == 400 and rnd.random() < 0.5:  # disjoint by construction
+            slots = [base + k * (nb + 16 * rnd.randrange(0, 4)) * 2 for k in range(2 * n)]
+        ins, outs = slots[:n], slots[n:]
+        if rnd.random() < 0.3:  # in place for some ranks
+            for r in range(n):
+                if rnd.random() < 0.5:
+                    outs[r] = ins[r]
+        want = pairwise(ins, outs, True)
+        seen[want] += 1
+        assert ar(vc, ins, outs, n, M) == want, (trial, n)
+    assert seen[ALIAS] > 100 and seen[CUDA] > 100, seen
+    # ReduceScatter: outputs of q elements against inputs of M, never in place
+    for trial in range(200):
+        n = rnd.choice([2, 4, 8])
+        q = -(-M // n)
+        ins = [base + k * nb * 3 for k in range(n)]
+        outs = [base + (1 << 30) + k * q * es for k in range(n)]
+        if trial % 2:
+            r = rnd.randrange(n)
+            outs[r] = ins[rnd.randrange(n)] + 16 * rnd.randrange(0, nb // 16)
+        want = ALIAS if trial % 2 else CUDA
+        assert rs(vc, ins, outs, n, M) == want, trial

@@ -52,3 +52,41 @@ def test_aggregate_over_two_gloo_ranks():
     for rank, ms, total in got:
         assert ms == 15.0          # the slower rank's time
         assert total == 3000       # every rank's bytes
+
+
+def _worker_lost_peer(rank, world, port, q):
+    import datetime
+    import time
+
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        os._exit(0)  # leaves between steps, without joining the collective
+    t0 = time.monotonic()
+    try:
+        bench.aggregate(torch, 10.0, 1000, world)
+        q.put(("returned", time.monotonic() - t0))
+    except Exception as e:  # noqa: BLE001 - any error is the expected outcome
+        q.put(("raised", time.monotonic() - t0, type(e).__name__))
+
+
+def test_lost_rank_ends_the_collective_with_an_error():
+    """A rank that leaves between steps: the other rank's next collective
+    fails within the process-group timeout instead of waiting forever."""
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_worker_lost_peer, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = q.get(timeout=120)
+    for p in procs:
+        p.join(60)
+        if p.is_alive():
+            p.kill()
+    assert out[0] == "raised", out
+    assert out[1] < 60, out

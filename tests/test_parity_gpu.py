@@ -596,3 +596,40 @@ def test_prepared_calls_match_direct_calls(env):
             assert_bits_equal(to_host(y2[r], "float32"), oy[r], "float32", "prepared dec")
             assert_bits_equal(to_host(g[r], "float32"), oy[r], "float32", "prepared AG")
             assert_bits_equal(to_host(z[r], "float32"), oz[r], "float32", "prepared RS")
+
+
+def test_prepared_calls_replay_from_a_cuda_graph(env):
+    """The collectives only enqueue work on the stream they are given (no
+    synchronisation, no allocation), so prepared calls can be captured in a
+    CUDA graph and replayed on new inputs written into the same buffers."""
+    vc, torch = env.vc, env.torch
+    n, M = 8, 200_003
+    q = vc.vc_shard_count(M, n)
+    d = [torch.empty(M, device=env.dev) for _ in range(n)]
+    y = [torch.empty(M, device=env.dev) for _ in range(n)]
+    y2 = [torch.empty(M, device=env.dev) for _ in range(n)]
+    z = [torch.empty(q, device=env.dev) for _ in range(n)]
+    sh = [torch.empty(q, device=env.dev) for _ in range(n)]
+    calls = [vc.prepare_all_reduce(d, y, order="ring"),
+             vc.prepare_reduce_scatter(d, z, order="recursive_halving"),
+             vc.prepare_all_reduce_decomposed(d, sh, y2, order="pairwise_tree")]
+    for c in calls:  # first calls outside capture (per-device queries are cached)
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    for seed in (31, 32):
+        xs = gen("float32", n, M, seed=seed)
+        for t, x in zip(d, xs):
+            t.copy_(torch.from_numpy(x))
+        g.replay()
+        torch.cuda.synchronize()
+        oy = oracle.all_reduce(xs, "float32", "sum", "ring")
+        oz = oracle.reduce_scatter(xs, "float32", "sum", "recursive_halving")
+        ot = oracle.all_reduce(xs, "float32", "sum", "pairwise_tree")
+        for r in range(n):
+            assert_bits_equal(to_host(y[r], "float32"), oy[r], "float32", "graph AR")
+            assert_bits_equal(to_host(z[r], "float32"), oz[r], "float32", "graph RS")
+            assert_bits_equal(to_host(y2[r], "float32"), ot[r], "float32", "graph dec")
