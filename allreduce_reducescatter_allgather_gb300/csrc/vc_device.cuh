@@ -668,6 +668,10 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
             }
         }
     }
+    // This block is done: a kernel launched after this one with programmatic
+    // stream serialization may start now (it waits for the whole grid, and
+    // for its memory, before it touches any; see vc_ag_kernel).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ReduceScatter: index space [0, N*q), one store per element into the shard
@@ -742,6 +746,13 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
     using U = typename Bits<ES>::U;
     constexpr int V = 16 / ES;
     constexpr int S = kGatherSlots;
+    // Launched with programmatic stream serialization, this grid may begin
+    // while the kernel before it (the ReduceScatter of a decomposed
+    // AllReduce) finishes; wait for that grid to complete and its writes to
+    // be visible before the first access to global memory.  (Launched
+    // normally, or after a kernel that never signals, this returns at once
+    // or when that kernel has completed.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long nvec = (p.M + V - 1) / V;
     const long long span = (long long)blockDim.x * S;
     const int r0 = (int)blockIdx.y * p.rpg;
