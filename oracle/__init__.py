@@ -34,7 +34,8 @@ ORDERS = {"ring": 0, "recursive_halving": 1, "pairwise_tree": 2, "sequential": 3
 NP_STORAGE = {"int32": np.int32, "int64": np.int64, "float32": np.float32,
               "bfloat16": np.uint16}
 
-_ERRORS = {-1: "bad argument", -2: "unsupported (order needs N = 2^k)", -3: "no memory"}
+_ERRORS = {-1: "bad argument", -2: "unsupported (recursive halving needs N = 2^k)",
+           -3: "no memory"}
 
 
 class OracleError(RuntimeError):

@@ -197,13 +197,14 @@ def recursive_halving_reduce_scatter(bufs, op: str = "sum"):
 
 def tree_parent(r: int, n: int) -> int:
     """Parent of rank r in the tree of the figure: rank r's level is its lowest
-    set bit L; its parent is (r - L) | 2L, and the top of that chain, which
-    would be N, is rank 0 (the root with a single child)."""
+    set bit L; its parent is (r - L) | 2L.  When that label is not a rank
+    (>= N) the parent is r - L: for N = 2^k only rank N/2 is in that case,
+    and it hangs under rank 0, the root with a single child."""
     if r == 0:
         return -1
     low = r & -r
     p = (r - low) | (low << 1)
-    return p if p < n else 0
+    return p if p < n else r - low
 
 
 def tree_reduce_broadcast(bufs, op: str = "sum"):
@@ -240,24 +241,30 @@ def tree_reduce_broadcast(bufs, op: str = "sum"):
     return [result.copy() for _ in range(n)], parents, reduce_rounds + bcast_rounds
 
 
+def tree_b_node(k: int, n: int) -> int:
+    """The rank that plays node k of the first tree in the second one: k + 1
+    mod n for even n (the rank numbers shifted by one), n - 1 - k for odd n
+    (the mirror image)."""
+    return (k + 1) % n if n % 2 == 0 else n - 1 - k
+
+
 def tree_b_parent(r: int, n: int) -> int:
-    """Parent of rank r in the second tree of a double binary tree: the
-    first tree with every rank number shifted by one (even n)."""
-    p = tree_parent((r - 1) % n, n)
-    return -1 if p == -1 else (p + 1) % n
+    """Parent of rank r in the second tree of a double binary tree."""
+    k = next(k for k in range(n) if tree_b_node(k, n) == r)
+    p = tree_parent(k, n)
+    return -1 if p == -1 else tree_b_node(p, n)
 
 
 def double_tree_reduce_broadcast(bufs, op: str = "sum"):
     """Each rank's buffer is cut in two halves (the first ceil(M/2)
     elements, the rest); the first half is reduced and broadcast over the
-    tree, the second over the shifted tree.  Returns (outputs, parents of
-    tree B)."""
+    tree, the second over tree B.  Returns (outputs, parents of tree B)."""
     n = len(bufs)
     M = np.asarray(bufs[0]).size
     h = (M + 1) // 2
     first = [np.asarray(b)[:h] for b in bufs]
-    # tree B: node k of the plain tree is played by rank (k+1) mod n
-    second = [np.asarray(bufs[(k + 1) % n])[h:] for k in range(n)]
+    # tree B: node k of the plain tree is played by rank tree_b_node(k)
+    second = [np.asarray(bufs[tree_b_node(k, n)])[h:] for k in range(n)]
     out_a, _, _ = tree_reduce_broadcast(first, op)
     out_b, _, _ = tree_reduce_broadcast(second, op)
     outs = [np.concatenate([out_a[r], out_b[r]]) for r in range(n)]

@@ -30,9 +30,11 @@
  *    (0,1)... for N=8); needs N = 2^k.
  *  - tree: "通信与互联（01）" 六.1 figure: rank 0 is the root with one child,
  *    a rank's level is the lowest set bit of its number, odd ranks are leaves;
- *    an inner node receives both children, adds itself, sends to its parent.
- *  - double binary tree: same page, 六.3: two trees, the second the first with
- *    every rank number shifted by one; each carries half of the data.
+ *    an inner node receives both children, adds itself, sends to its parent;
+ *    the tree is binary and takes 2*ceil(log2 N) steps.
+ *  - double binary tree: same page, 六.3: two trees, each carrying half of the
+ *    data; for even N the second is the first with every rank number shifted
+ *    by one, for odd N its mirror image.
  *
  * Readings where the pages are silent (each one is also listed in the design
  * notes):
@@ -47,9 +49,15 @@
  *  - tree inner node: (left subtree (+) right subtree) (+) own value, the
  *    lower-numbered child on the left (parity unpinned: the pages fix only
  *    the tree's shape);
- *  - recursive halving and tree are defined for N a power of two only;
+ *  - recursive halving is defined for N a power of two only;
+ *  - tree with N not a power of two: a rank whose parent label (r - L) | 2L
+ *    is not a rank (>= N) hangs under r - L instead.  This keeps what the
+ *    figure states for every N (a binary tree, a root with one child, odd
+ *    ranks as leaves, depth ceil(log2 N)), and it is the tree of the next
+ *    power of two with the missing ranks passing their one subtree through;
  *  - double binary tree: tree A reduces the first ceil(M/2) elements of the
- *    buffer, tree B (ranks shifted by one) the rest, padding included.
+ *    buffer, tree B the rest, padding included; in tree B node k is played
+ *    by rank (k+1) mod N (even N) or N-1-k (odd N).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math).
  */
@@ -291,13 +299,14 @@ static val_t fold_recursive_halving(int op, const val_t *a, int n, int owner)
 }
 
 /* Tree shape: a rank's level is its lowest set bit L; its parent is the rank
- * one level up whose subtree contains it, (r - L) | 2L; rank N/2 hangs under
- * the root, rank 0. */
+ * one level up whose subtree contains it, (r - L) | 2L.  Where that label is
+ * not a rank (>= N) the parent is r - L: with N = 2^k this happens only for
+ * rank N/2, which hangs under the root, rank 0. */
 static int tree_parent(int r, int n)
 {
     int low = r & -r;
     int p = (r - low) | (low << 1);
-    return p < n ? p : 0;
+    return p < n ? p : r - low;
 }
 
 typedef struct {
@@ -346,8 +355,7 @@ static int plan_init(plan_t *pl, int n, int64_t M, int dtype, int op, int order)
         return OR_BAD_ARGUMENT;
     if (order < OR_RING || order > OR_DOUBLE_TREE)
         return OR_BAD_ARGUMENT;
-    if ((order == OR_RECURSIVE_HALVING || order == OR_PAIRWISE_TREE ||
-         order == OR_DOUBLE_TREE) && !is_pow2(n))
+    if (order == OR_RECURSIVE_HALVING && !is_pow2(n))
         return OR_UNSUPPORTED;
     pl->n = n;
     pl->M = M;
@@ -373,10 +381,11 @@ static val_t reduce_operands(const plan_t *pl, const val_t *a, int64_t i)
         if (i < (pl->M + 1) / 2) {
             v = fold_tree_node(pl->op, a, &pl->tree, 0); /* tree A */
         } else {
-            /* tree B: the same tree with node k played by rank (k+1) mod N */
+            /* tree B: the same tree with node k played by rank (k+1) mod N
+             * (even N) or by rank N-1-k (odd N) */
             val_t b[OR_MAX_RANKS];
             for (int k = 0; k < pl->n; ++k)
-                b[k] = a[(k + 1) % pl->n];
+                b[k] = a[(pl->n % 2 == 0) ? (k + 1) % pl->n : pl->n - 1 - k];
             v = fold_tree_node(pl->op, b, &pl->tree, 0);
         }
         break;

@@ -24,6 +24,12 @@ ALL_ORDERS = ORDERS + ["sequential"]
 OPS = ["sum", "prod", "max", "min", "avg"]
 
 
+def _orders_for(n, orders):
+    """The orders defined for N ranks: all but recursive halving unless N is a
+    power of two."""
+    return [o for o in orders if n & (n - 1) == 0 or o != "recursive_halving"]
+
+
 def lin(n, M, dtype="int64"):
     return si.generate(dtype, "rank_linear", n, M, seed=0)
 
@@ -299,7 +305,7 @@ def test_tree_shape_n8():
     assert leaves == ints(g["leaves"])
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16, 33, 64])
 @pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
 def test_tree_replay_equals_oracle_fold(n, op):
     """Reduce-then-broadcast over the tree gives every rank the oracle's
@@ -316,14 +322,117 @@ def test_tree_replay_equals_oracle_fold(n, op):
 
 
 @pytest.mark.parametrize("n", [3, 5, 6, 12])
-def test_hypercube_orders_need_power_of_two(n):
+def test_recursive_halving_needs_power_of_two(n):
     """Recursive halving needs N = 2^k ("ReduceScatter" page, algorithm table:
-    hypercube); the tree order is read the same way.  The ring takes any N."""
+    hypercube).  The ring and both tree orders take any N."""
     xs = si.generate("float32", "uniform_pm1", n, 10, seed=n)
-    for order in ("recursive_halving", "pairwise_tree"):
-        with pytest.raises(oracle.OracleError):
-            oracle.all_reduce(xs, "float32", "sum", order)
-    oracle.all_reduce(xs, "float32", "sum", "ring")
+    with pytest.raises(oracle.OracleError):
+        oracle.all_reduce(xs, "float32", "sum", "recursive_halving")
+    for order in ("ring", "pairwise_tree", "double_binary_tree"):
+        oracle.all_reduce(xs, "float32", "sum", order)
+
+
+# ------------------------------------------------- trees for any rank count --
+
+def _children(parents):
+    kids = {r: [] for r in range(len(parents))}
+    for r, p in enumerate(parents):
+        if p >= 0:
+            kids[p].append(r)
+    return kids
+
+
+def _depth(parents, r):
+    d = 0
+    while parents[r] >= 0:
+        r = parents[r]
+        d += 1
+        assert d <= len(parents), "cycle"
+    return d
+
+
+@pytest.mark.parametrize("n", range(1, 65))
+def test_tree_shape_any_n_keeps_the_figures_properties(n):
+    """For every N the tree keeps what "通信与互联（01）" 六.1 states of it:
+    rank 0 is the root and has a single child, the tree is binary, odd ranks
+    are exactly the leaves, a rank's level (lowest set bit) grows towards the
+    root, and the depth is ceil(log2 N), so reduce + broadcast take
+    2*ceil(log2 N) steps.  A fallback that hung orphans on the root would
+    give it several children (N = 6: ranks 4 and 5)."""
+    parents = [int(p) for p in oracle.tree_parents(n)]
+    assert parents == [sim.tree_parent(r, n) for r in range(n)]
+    assert parents[0] == -1
+    kids = _children(parents)
+    if n == 1:
+        return
+    assert len(kids[0]) == 1
+    assert all(len(k) <= 2 for k in kids.values())
+    assert [r for r in range(n) if not kids[r]] == [r for r in range(n) if r % 2 == 1]
+    for r in range(1, n):
+        p = parents[r]
+        assert p == 0 or (p & -p) > (r & -r)
+        # in-order labels, as in the figure: a lower child on the left, a
+        # higher one on the right
+        assert len([c for c in kids[r] if c < r]) <= 1 and len([c for c in kids[r] if c > r]) <= 1
+    assert max(_depth(parents, r) for r in range(n)) == math.ceil(math.log2(n))
+
+
+def test_tree_non_power_of_two_hand_tables():
+    g = read_golden("tree_non_pow2.txt")
+    for n in (5, 6, 12):
+        assert [int(p) for p in oracle.tree_parents(n)] == ints(g[f"parents_{n}"])
+    for n in (5, 6):
+        assert [sim.tree_b_parent(r, n) for r in range(n)] == ints(g[f"parents_b_{n}"])
+
+
+def test_tree_non_power_of_two_hand_values():
+    """Hand-rounded fp32 sums that tell the tree from the ring, the parent
+    fallback r - L from a fallback to the root, and the odd-N mirror tree B
+    from a shifted one."""
+    g = read_golden("tree_non_pow2.txt")
+    for n, keys in ((6, ("tree", "tree_b")), (5, ("tree", "tree_b"))):
+        a = [np.float32(v) for v in ints(g[f"n{n}_operands"])]
+        xs = [np.array([v, v], np.float32) for v in a]  # M = 2: one element per tree
+        y = oracle.all_reduce(xs, "float32", "sum", "pairwise_tree")[0]
+        assert _bits(y[0]) == int(g[f"n{n}_tree"], 0)
+        d = oracle.all_reduce(xs, "float32", "sum", "double_binary_tree")[0]
+        assert [_bits(v) for v in d] == [int(g[f"n{n}_tree"], 0), int(g[f"n{n}_tree_b"], 0)]
+    a = [np.float32(v) for v in ints(g["n6_operands"])]
+    xs = [np.array([v], np.float32) for v in a]
+    assert _bits(oracle.all_reduce(xs, "float32", "sum", "ring")[0][0]) == int(g["n6_ring"], 0)
+
+
+_PAD = {"sum": 0.0, "prod": 1.0, "max": -np.inf, "min": np.inf}
+
+
+@pytest.mark.parametrize("n", [3, 5, 6, 7, 9, 12, 17, 24, 33, 63])
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
+def test_tree_non_power_of_two_is_the_padded_power_of_two_tree(n, op):
+    """The tree over N ranks equals, bit for bit, the tree over the next
+    power of two P (pinned by the figure) with ranks N..P-1 holding the op's
+    identity: a missing rank only passes its one subtree through, and
+    x (+) e = x exactly for every finite x other than -0."""
+    P = 1 << (n - 1).bit_length()
+    M = 37
+    xs = si.generate("float32", "uniform_pm1", n, M, seed=400 + n)
+    if op == "prod":
+        xs = [np.float32(1.0) + x * np.float32(0.25) for x in xs]
+    pad = [np.full(M, _PAD[op], np.float32) for _ in range(P - n)]
+    y = oracle.all_reduce(xs, "float32", op, "pairwise_tree")[0]
+    yp = oracle.all_reduce(xs + pad, "float32", op, "pairwise_tree")[0]
+    np.testing.assert_array_equal(y.view(np.uint32), yp.view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [2, 4, 6, 10, 12, 14, 30, 62])
+def test_double_tree_even_n_swaps_leaves_and_inner_nodes(n):
+    """For even N the shifted second tree makes A's leaves B's inner nodes and
+    the reverse ("通信与互联（01）" 六.3), at every even N, not only N = 8."""
+    pa = [int(p) for p in oracle.tree_parents(n)]
+    pb = [sim.tree_b_parent(r, n) for r in range(n)]
+    inner_a = set(p for p in pa if p >= 0)
+    leaves_b = set(range(n)) - set(p for p in pb if p >= 0)
+    assert inner_a == leaves_b
+    assert pb.count(-1) == 1 and pb.index(-1) == 1
 
 
 def test_step_counts():
@@ -360,7 +469,7 @@ def test_float_sums_within_rounding_bound_of_exact(n):
     absum = sum(np.abs(x.astype(np.float64)) for x in xs)
     bound = _gamma(n - 1) * absum
     results = {}
-    orders = ALL_ORDERS if n & (n - 1) == 0 else ["ring", "sequential"]
+    orders = _orders_for(n, ALL_ORDERS)
     for order in orders:
         y = oracle.all_reduce(xs, "float32", "sum", order)[0].astype(np.float64)
         assert np.all(np.abs(y - exact) <= bound), order
@@ -377,7 +486,7 @@ def test_avg_is_sum_divided_once(n):
     separates this from multiplying by a rounded 1/N."""
     M = 4000
     xs = si.generate("float32", "uniform_pm1", n, M, seed=9)
-    orders = ORDERS if n & (n - 1) == 0 else ["ring"]
+    orders = _orders_for(n, ORDERS)
     for order in orders:
         s = oracle.all_reduce(xs, "float32", "sum", order)[0]
         a = oracle.all_reduce(xs, "float32", "avg", order)[0]
@@ -437,7 +546,7 @@ def test_integer_ops_wraparound_and_order_free(dtype, n):
             # C division truncates toward zero (no overflow at these sizes)
             "avg": np.trunc(wide.sum(axis=0) / n).astype(np.int64),
         }
-    orders = ALL_ORDERS if n & (n - 1) == 0 else ["ring", "sequential"]
+    orders = _orders_for(n, ALL_ORDERS)
     for op in OPS:
         outs = [oracle.all_reduce(xs, dtype, op, order)[0] for order in orders]
         for o in outs[1:]:
@@ -585,7 +694,7 @@ def test_double_tree_shape_n8():
     assert inner_a == leaves_b
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16, 33, 64])
 @pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
 def test_double_tree_replay_equals_oracle(n, op):
     """Halves reduced over the tree and the shifted tree, replayed, equal the
