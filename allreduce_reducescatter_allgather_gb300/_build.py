@@ -22,13 +22,16 @@ LIB = LIBDIR / "libvc.so"
 
 SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu", "vc_copy.cu"]
 HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
-# vc_reduce_inst.cu compiled once per (element type, op): (object, -D flags)
+# vc_reduce_inst.cu compiled once per (element type, op, order group):
+# (object, -D flags).  Groups: 0 ring + recursive halving, 1 tree, 2 double
+# binary tree.
 INSTANCE_SOURCE = "vc_reduce_inst.cu"
 _TYPES = {"i32": "int32_t", "i64": "long long", "f32": "float", "bf16": "__nv_bfloat16"}
 _OPS = {"sum": "OpSum", "prod": "OpProd", "max": "OpMax", "min": "OpMin"}
-INSTANCES = [(f"vc_reduce_{t}_{o}", [f"-DVC_T={ct}", f"-DVC_OP={op}",
-                                     f"-DVC_FN=launch_reduce_{t}_{o}"])
-             for t, ct in _TYPES.items() for o, op in _OPS.items()]
+_GROUPS = (0, 1, 2)
+INSTANCES = [(f"vc_reduce_{t}_{o}_g{g}", [f"-DVC_T={ct}", f"-DVC_OP={op}", f"-DVC_GROUP={g}",
+                                          f"-DVC_FN=launch_reduce_{t}_{o}_g{g}"])
+             for t, ct in _TYPES.items() for o, op in _OPS.items() for g in _GROUPS]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
@@ -75,8 +78,9 @@ def build_library(force: bool = False, jobs: int | None = None) -> Path:
 
     jobs_list = [(Path(s).stem, s, []) for s in SOURCES]
     jobs_list += [(stem, INSTANCE_SOURCE, defs) for stem, defs in INSTANCES]
-    # the largest slices first, so the pool finishes together
-    jobs_list.sort(key=lambda j: 0 if j[1] == INSTANCE_SOURCE else 1)
+    # the largest slices first (double tree, tree, ring), so the pool
+    # finishes together
+    jobs_list.sort(key=lambda j: -int(j[0][-1]) if j[1] == INSTANCE_SOURCE else 1)
     jobs = jobs or max(1, os.cpu_count() or 4)
     with ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(compile_one, jobs_list))

@@ -35,7 +35,6 @@ bool valid_op(vc_op_t op) { return op >= VC_SUM && op <= VC_AVG; }
 bool valid_order(vc_order_t o) {
     return o >= VC_ORDER_RING && o <= VC_ORDER_DOUBLE_BINARY_TREE;
 }
-bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
 // Common checks of every call.  *bytes_m and *bytes_q receive the byte sizes
 // of a full rank buffer (M elements) and of a shard (q elements).
@@ -279,7 +278,7 @@ vc_status_t vc_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
     vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
     if (s != VC_SUCCESS) return s;
     if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
-    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (order == VC_ORDER_RECURSIVE_HALVING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
     if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
@@ -308,7 +307,7 @@ vc_status_t vc_all_reduce(const void* const* sendbufs, void* const* recvbufs, in
     vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
     if (s != VC_SUCCESS) return s;
     if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
-    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (order == VC_ORDER_RECURSIVE_HALVING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
     if ((s = check_table(recvbufs, nranks, dtype)) != VC_SUCCESS) return s;
@@ -325,7 +324,7 @@ vc_status_t vc_all_reduce_decomposed(const void* const* sendbufs, void* const* s
     vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
     if (s != VC_SUCCESS) return s;
     if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
-    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (order == VC_ORDER_RECURSIVE_HALVING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
     if ((s = check_table(shardbufs, nranks, dtype)) != VC_SUCCESS) return s;
@@ -349,7 +348,7 @@ vc_status_t vc_reduce(const void* const* sendbufs, void* recvbuf, int nranks, si
     vc_status_t s = check_shape(nranks, count, dtype, &bm, &bq);
     if (s != VC_SUCCESS) return s;
     if (!valid_op(op) || !valid_order(order)) return VC_ERR_INVALID_ARGUMENT;
-    if (order != VC_ORDER_RING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
+    if (order == VC_ORDER_RECURSIVE_HALVING && !is_pow2(nranks)) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     if ((s = check_table(sendbufs, nranks, dtype)) != VC_SUCCESS) return s;
     void* const out[1] = {recvbuf};
@@ -394,7 +393,7 @@ const char* vc_status_string(vc_status_t status) {
     switch (status) {
     case VC_SUCCESS: return "success";
     case VC_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case VC_ERR_UNSUPPORTED: return "unsupported: this order needs a power-of-two rank count";
+    case VC_ERR_UNSUPPORTED: return "unsupported: recursive halving needs a power-of-two rank count";
     case VC_ERR_ALIAS: return "an output buffer overlaps an input or another output";
     case VC_ERR_CUDA: return "CUDA launch failed";
     default: return "unknown status";

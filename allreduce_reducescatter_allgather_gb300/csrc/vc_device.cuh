@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace vc {
 
 constexpr int kMaxRanks = 64;
@@ -152,6 +154,58 @@ __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) {
 __device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
+// 16 bytes at an address aligned only to the element size ES (a shard whose
+// start is not on a 16-byte boundary): the widest accesses the address
+// allows, 16, 8, 4 or 2 bytes.  Little-endian: byte 0 is the low byte of x.
+template <int ES>
+__device__ __forceinline__ void st_aligned(void* p, const uint4& v) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if ((a & 15) == 0) {
+        st16(p, v);
+    } else if (ES >= 8 || (a & 7) == 0) {
+        uint2* d = static_cast<uint2*>(p);
+        d[0] = make_uint2(v.x, v.y);
+        d[1] = make_uint2(v.z, v.w);
+    } else if (ES >= 4 || (a & 3) == 0) {
+        unsigned* d = static_cast<unsigned*>(p);
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+    } else {
+        unsigned short* d = static_cast<unsigned short*>(p);
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            d[2 * k] = (unsigned short)(w[k] & 0xffffu);
+            d[2 * k + 1] = (unsigned short)(w[k] >> 16);
+        }
+    }
+}
+
+template <int ES>
+__device__ __forceinline__ uint4 ld_aligned(const void* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    uint4 v;
+    if ((a & 15) == 0) {
+        v = ld16(p);
+    } else if (ES >= 8 || (a & 7) == 0) {
+        const uint2* s = static_cast<const uint2*>(p);
+        const uint2 lo = s[0], hi = s[1];
+        v = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    } else if (ES >= 4 || (a & 3) == 0) {
+        const unsigned* s = static_cast<const unsigned*>(p);
+        v = make_uint4(s[0], s[1], s[2], s[3]);
+    } else {
+        const unsigned short* s = static_cast<const unsigned short*>(p);
+        unsigned w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = (unsigned)s[2 * k] | ((unsigned)s[2 * k + 1] << 16);
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return v;
+}
+
 // ------------------------------------------------------------------- ops --
 
 // a (+) b with the running value on the left.  Floats: one IEEE single
@@ -236,6 +290,7 @@ __device__ __forceinline__ long long avg_div(long long s, int n) { return s / (l
 // The 16-byte vector at element offset i0 of rank r.
 template <class T> struct VecLoader {
     using A = typename Traits<T>::Acc;
+    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const ReduceParams& p;
@@ -254,6 +309,7 @@ template <class T> struct VecLoader {
 // from M to N*q.
 template <class T, class Op> struct ScalarLoader {
     using A = typename Traits<T>::Acc;
+    using Elem = T;
     static constexpr int W = 1;
     using Raw = A;
     const ReduceParams& p;
@@ -273,6 +329,7 @@ template <class T, class Op> struct ScalarLoader {
 // whose rank index is only known at run time).
 template <class T> struct SharedTableLoader {
     using A = typename Traits<T>::Acc;
+    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const void* const* table;
@@ -291,6 +348,7 @@ template <class T> struct SharedTableLoader {
 // the thread's slot u.
 template <class T, int NR, int U> struct PreLoader {
     using A = typename Traits<T>::Acc;
+    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const uint4 (&buf)[NR][U];
@@ -305,14 +363,63 @@ template <class T, int NR, int U> struct PreLoader {
 
 template <class L> using VecOf = Vec<typename L::A, L::W>;
 
-// The second tree of a double binary tree: node k is played by rank
-// (k + 1) mod N, so every rank index stays a compile-time constant.
-template <class L, int N> struct ShiftedByOne {
+// The rank that plays node k of the tree in the second tree of a double
+// binary tree: k + 1 mod n for even n (rank numbers shifted by one), n-1-k
+// for odd n (the mirror image).
+__host__ __device__ constexpr int tree_b_rank(int k, int n) {
+    return (n % 2 == 0) ? (k + 1 == n ? 0 : k + 1) : n - 1 - k;
+}
+
+// The second tree with N known at compile time: every rank index stays a
+// compile-time constant.
+template <class L, int N> struct TreeBStatic {
     using A = typename L::A;
+    using Elem = typename L::Elem;
     static constexpr int W = L::W;
     using Raw = typename L::Raw;
     const L& l;
-    __device__ __forceinline__ Raw raw(int k) const { return l.raw((k + 1) % N); }
+    __device__ __forceinline__ Raw raw(int k) const { return l.raw(tree_b_rank(k, N)); }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
+};
+
+// The second tree with a run-time N (the rank index is computed).
+template <class L> struct TreeBRuntime {
+    using A = typename L::A;
+    using Elem = typename L::Elem;
+    static constexpr int W = L::W;
+    using Raw = typename L::Raw;
+    const L& l;
+    int n;
+    __device__ __forceinline__ Raw raw(int k) const { return l.raw(tree_b_rank(k, n)); }
+    __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
+};
+
+// Ranks n .. of a power-of-two envelope, holding the op's identity e (no
+// load).  For integers x (+) e = x exactly for every op, so the envelope's
+// tree over the padded ranks gives the same value, bit for bit, as the tree
+// over n ranks in which a missing rank passes its one subtree through: a
+// node with a missing right subtree computes (l (+) e) (+) own = l (+) own,
+// and a missing node (l (+) e) (+) e = l.  (Floats are not padded this way:
+// -0 (+) +0 is +0.)  The padded tree has no branches, so the compiler can
+// schedule every load early.
+template <class L, class Op> struct IdentityPadded {
+    using A = typename L::A;
+    static constexpr int W = L::W;
+    using Raw = typename L::Raw;
+    using Elem = typename L::Elem;
+    const L& l;
+    int n;
+    __device__ __forceinline__ static Raw identity() {
+        if constexpr (W == 1) {
+            return Identity<Elem, Op>::get();
+        } else {
+            Vec<A, W> e;
+#pragma unroll
+            for (int k = 0; k < W; ++k) e.x[k] = Identity<Elem, Op>::get();
+            return pack(e, (Elem*)nullptr);
+        }
+    }
+    __device__ __forceinline__ Raw raw(int k) const { return k < n ? l.raw(k) : identity(); }
     __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
 };
 
@@ -341,6 +448,49 @@ __device__ __forceinline__ VecOf<L> fold_ring(const L& ld, int n_rt, int c) {
         for (int u = 0; u < G; ++u)
             if (k0 + u < n && k0 + u > 0) acc = vop<Op>(acc, ld.cvt(t[u]));
     }
+    return acc;
+}
+
+// Ring with a run-time N, read from a doubled pointer table (entry k holds
+// rank k mod N), so the ranks c, c+1, ..., c+N-1 of chunk c are the entries
+// c .. c+N-1 and need no wrap-around.  Whole groups of kGroup entries, then
+// one group of the remaining N mod kGroup; each group's loads are all issued
+// before it is folded, and no load needs a guard.
+template <class Op, int R, class L>
+__device__ __forceinline__ void ring_run(const L& ld, int k, VecOf<L>& acc, bool first) {
+    typename L::Raw t[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) t[u] = ld.raw(k + u);
+    if (first)
+        acc = ld.cvt(t[0]);
+    else
+        acc = vop<Op>(acc, ld.cvt(t[0]));
+#pragma unroll
+    for (int u = 1; u < R; ++u) acc = vop<Op>(acc, ld.cvt(t[u]));
+}
+
+template <class Op, int R, class L>
+__device__ __forceinline__ void ring_tail(const L& ld, int k, int rem, VecOf<L>& acc, bool first) {
+    if constexpr (R > 0) {
+        if (rem == R)
+            ring_run<Op, R>(ld, k, acc, first);
+        else
+            ring_tail<Op, R - 1>(ld, k, rem, acc, first);
+    }
+}
+
+template <class Op, class L>
+__device__ __forceinline__ VecOf<L> fold_ring_doubled(const L& ld, int n, int c) {
+    VecOf<L> acc;
+    const int end = c + n;
+    int k = c;
+    bool first = true;
+#pragma unroll 1
+    for (; k + kGroup <= end; k += kGroup) {
+        ring_run<Op, kGroup>(ld, k, acc, first);
+        first = false;
+    }
+    ring_tail<Op, kGroup - 1>(ld, k, end - k, acc, first);
     return acc;
 }
 
@@ -451,6 +601,93 @@ __device__ __forceinline__ VecOf<Ld> fold_tree(const Ld& ld) {
     }
 }
 
+// Trees over n ranks, n not a power of two: the tree of the next power of
+// two PT with ranks n .. PT-1 missing.  A node whose own rank is missing has
+// nothing in its right subtree either, and passes its left subtree's value
+// through; a present node whose right subtree is empty combines its left
+// subtree with its own operand.  This is the tree in which a rank whose
+// parent label (r - L) | 2L is not a rank hangs under r - L.  Each function
+// is called only for a subtree that holds at least one rank.  With n a
+// compile-time constant every test folds away; with a run-time n they are
+// uniform branches.
+
+// t[K] holds rank BASE + K (absent ranks are never read).
+template <class Op, int K, int L, class Ld, class R, int G>
+__device__ __forceinline__ VecOf<Ld> tree_local_n(const Ld& ld, const R (&t)[G], int base, int n) {
+    if constexpr (L == 1) {
+        return ld.cvt(t[K]);
+    } else {
+        const int P = base + K;
+        VecOf<Ld> l = tree_local_n<Op, K - L / 2, L / 2>(ld, t, base, n);
+        if (P >= n) return l;
+        if (P + 1 >= n) return vop<Op>(l, ld.cvt(t[K]));
+        VecOf<Ld> r = tree_local_n<Op, K + L / 2, L / 2>(ld, t, base, n);
+        return vop<Op>(vop<Op>(l, r), ld.cvt(t[K]));
+    }
+}
+
+// Block B of 16 ranks, as in tree_block, with the ranks from n on skipped.
+template <class Op, int B, class Ld>
+__device__ __forceinline__ VecOf<Ld> tree_block_n(const Ld& ld, typename Ld::Raw& first, int n) {
+    typename Ld::Raw t[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t[k] = (16 * B + k < n) ? ld.raw(16 * B + k) : typename Ld::Raw{};
+    first = t[0];
+    return tree_local_n<Op, 8, 8>(ld, t, 16 * B, n);
+}
+
+// T(P) for a node of level L >= 8, as in tree_upper.
+template <class Op, int P, int L, class Ld>
+__device__ __forceinline__ VecOf<Ld> tree_upper_n(const Ld& ld, typename Ld::Raw& first, int n) {
+    if constexpr (L == 8) {
+        return tree_block_n<Op, (P - 8) / 16>(ld, first, n);
+    } else {
+        VecOf<Ld> l = tree_upper_n<Op, P - L / 2, L / 2>(ld, first, n);
+        if (P >= n) return l;
+        if (P + 1 >= n) return vop<Op>(l, ld.cvt(ld.raw(P)));
+        typename Ld::Raw own;
+        VecOf<Ld> r = tree_upper_n<Op, P + L / 2, L / 2>(ld, own, n);
+        return vop<Op>(vop<Op>(l, r), ld.cvt(own));
+    }
+}
+
+// The root, rank 0, with the single child PT/2 (n >= 2).
+template <class Op, int PT, class Ld>
+__device__ __forceinline__ VecOf<Ld> fold_tree_n(const Ld& ld, int n) {
+    static_assert(PT >= 4 && (PT & (PT - 1)) == 0, "envelope must be a power of two >= 4");
+    if constexpr (PT >= 16) {
+        typename Ld::Raw own0;
+        VecOf<Ld> t = tree_upper_n<Op, PT / 2, PT / 2>(ld, own0, n);
+        return vop<Op>(t, ld.cvt(own0));
+    } else {
+        typename Ld::Raw t[PT];
+#pragma unroll
+        for (int k = 0; k < PT; ++k) t[k] = (k < n) ? ld.raw(k) : typename Ld::Raw{};
+        return vop<Op>(tree_local_n<Op, PT / 2, PT / 2>(ld, t, 0, n), ld.cvt(t[0]));
+    }
+}
+
+__host__ __device__ constexpr bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+__host__ __device__ constexpr int pow2_ceil(int n) { return n <= 1 ? 1 : 2 * pow2_ceil((n + 1) / 2); }
+
+// One tree over the loader's ranks: NT > 0 a compile-time N (a power of two
+// takes the plain tree), NT < 0 a run-time n inside the envelope -NT.
+template <class Op, int NT, class Ld>
+__device__ __forceinline__ VecOf<Ld> fold_any_tree(const Ld& ld, int n) {
+    if constexpr (NT < 0 && sizeof(typename Ld::A) == 8) {
+        // integers: the plain tree of the envelope over identity-padded ranks
+        // (exact, see IdentityPadded)
+        IdentityPadded<Ld, Op> padded{ld, n};
+        return fold_tree<Op, -NT>(padded);
+    } else if constexpr (NT < 0) {
+        return fold_tree_n<Op, -NT>(ld, n);
+    } else if constexpr (is_pow2(NT)) {
+        return fold_tree<Op, NT>(ld);
+    } else {
+        return fold_tree_n<Op, (pow2_ceil(NT) < 4 ? 4 : pow2_ceil(NT))>(ld, NT);
+    }
+}
+
 // Ring with N known at compile time: the left fold starting at rank C, with
 // every rank index a constant (operands may already sit in registers).
 template <class Op, int N, int C, class L>
@@ -472,9 +709,10 @@ __device__ __forceinline__ VecOf<L> ring_switch(const L& ld, int c) {
     }
 }
 
-// NT > 0: N is a compile-time constant; NT == 0: ring with a run-time N.
-// The ring switches among its rotations up to N = 8 and folds in groups
-// with run-time rank indices beyond.  `sel` is the ring's chunk, or for the
+// NT > 0: N is a compile-time constant; NT == 0: ring with a run-time N;
+// NT < 0: tree orders with a run-time N inside the envelope -NT.  The ring
+// switches among its rotations up to N = 8 and folds in groups with
+// run-time rank indices beyond.  `sel` is the ring's chunk, or for the
 // double binary tree which tree (0 = A, 1 = B) the element belongs to.
 template <class Op, int ORDER, int NT, class L>
 __device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int sel) {
@@ -482,11 +720,16 @@ __device__ __forceinline__ VecOf<L> fold(const L& ld, int n, int sel) {
     if constexpr (ORDER == kOrderRecursiveHalving) {
         return rh_group<Op, 0, 1, NT>(ld);
     } else if constexpr (ORDER == kOrderPairwiseTree) {
-        return fold_tree<Op, NT>(ld);
+        return fold_any_tree<Op, NT>(ld, n);
     } else if constexpr (ORDER == kOrderDoubleTree) {
-        if (sel == 0) return fold_tree<Op, NT>(ld);
-        ShiftedByOne<L, NT> shifted{ld};
-        return fold_tree<Op, NT>(shifted);
+        if (sel == 0) return fold_any_tree<Op, NT>(ld, n);
+        if constexpr (NT > 0) {
+            TreeBStatic<L, NT> b{ld};
+            return fold_any_tree<Op, NT>(b, NT);
+        } else {
+            TreeBRuntime<L> b{ld, n};
+            return fold_any_tree<Op, NT>(b, n);
+        }
     } else if constexpr (NT > 0 && NT <= 8) {
         return ring_switch<Op, NT, 0>(ld, c);
     } else {
@@ -522,12 +765,7 @@ __device__ __forceinline__ void store_result(const ReduceParams& p, int c, long 
     }
     if constexpr (RS) {
         T* dst = static_cast<T*>(p.out[c]) + (i0 - (long long)c * p.q);
-        if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-            st16(dst, pack(acc, (T*)nullptr));
-        } else {
-#pragma unroll
-            for (int k = 0; k < V; ++k) store1(dst + k, acc.x[k]);
-        }
+        st_aligned<sizeof(T)>(dst, pack(acc, (T*)nullptr));
     } else {
         const uint4 u = pack(acc, (T*)nullptr);
         if constexpr (NT > 0) {
@@ -592,13 +830,20 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
     constexpr int V = Traits<T>::V;
     constexpr bool kPre = (NT > 0 && NT <= 8);
     // ring beyond 8 ranks: rotated rank indices read from shared memory
+    // (with a run-time N, a doubled input table: entry k is rank k mod N)
     constexpr bool kTable = (ORDER == kOrderRing && (NT == 0 || NT > 8));
-    __shared__ const void* s_in[kTable ? kMaxRanks : 1];
+    // trees with a run-time N: input pointers from shared memory (tree B
+    // computes its rank indices)
+    constexpr bool kTreeTable = (NT < 0);
+    constexpr int kInEntries = (kTable && NT == 0) ? 2 * kMaxRanks
+                                                    : ((kTable || kTreeTable) ? kMaxRanks : 1);
+    __shared__ const void* s_in[kInEntries];
     __shared__ void* s_out[kTable ? kMaxRanks : 1];
-    if constexpr (kTable) {
+    if constexpr (kTable || kTreeTable) {
         for (int r = threadIdx.x; r < p.n; r += blockDim.x) {
             s_in[r] = p.in[r];
-            s_out[r] = p.out[r];
+            if constexpr (kTable && NT == 0) s_in[r + p.n] = p.in[r];
+            if constexpr (kTable) s_out[r] = p.out[r];
         }
         __syncthreads();
     }
@@ -636,7 +881,11 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
             } else if constexpr (kTable) {
                 static_assert(U == 1, "streaming folds take one vector per thread");
                 SharedTableLoader<T> ld{s_in, v0 * V};
-                auto acc = fold<Op, ORDER, NT>(ld, p.n, c);
+                VecOf<SharedTableLoader<T>> acc;
+                if constexpr (NT == 0)
+                    acc = fold_ring_doubled<Op>(ld, p.n, c);
+                else
+                    acc = fold<Op, ORDER, NT>(ld, p.n, c);
                 if (p.avg) {
 #pragma unroll
                     for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
@@ -644,16 +893,16 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
                 const long long i0 = v0 * V;
                 if constexpr (RS) {
                     T* dst = static_cast<T*>(s_out[c]) + (i0 - (long long)c * p.q);
-                    if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                        st16(dst, pack(acc, (T*)nullptr));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < V; ++k) store1(dst + k, acc.x[k]);
-                    }
+                    st_aligned<sizeof(T)>(dst, pack(acc, (T*)nullptr));
                 } else {
                     const uint4 u = pack(acc, (T*)nullptr);
                     for (int s = 0; s < p.nout; ++s) st16(static_cast<T*>(s_out[s]) + i0, u);
                 }
+            } else if constexpr (kTreeTable) {
+                static_assert(U == 1, "streaming folds take one vector per thread");
+                SharedTableLoader<T> ld{s_in, v0 * V};
+                auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
+                store_result<T, NT, RS>(p, c, v0 * V, acc);
             } else {
                 static_assert(U == 1, "streaming folds take one vector per thread");
                 VecLoader<T> ld{p, v0 * V};
@@ -674,22 +923,38 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Resident blocks per SM the reduction kernels ask ptxas for.  Compile-time
+// N: one, stated explicitly.  Measured on GB300 against the bare launch
+// bound: ptxas then keeps more loads in flight per thread, which lifts
+// AllReduce by 0.5-1 % across the board and the 64-rank tree from 0.78x to
+// 1.06x the copy rate (the one loss measured: bf16 RS at 32 ranks in the
+// tree orders, 7.19 -> 6.54 TB/s).  Run-time N (folds that stream 16
+// operands at a time): two, so that a second block hides the first one's
+// load latency.  Measured: the ring at N = 12 from 0.81x to 0.96x (bf16
+// 0.67x to 0.82x); the padded int64 tree at N = 63 from 0.81x to 0.98x.
+// The exceptions keep one: int32 trees with a run-time N in the double
+// binary tree (at 128 registers it spills and fell from 0.72x to 0.62x) or
+// with PROD (64-bit products: hundreds of bytes of spills at 128).
+template <class T, class Op, int ORDER, int NT>
+constexpr int min_blocks() {
+    if (NT > 0) return 1;
+    constexpr bool int32_wide = sizeof(T) == 4 && sizeof(typename Traits<T>::Acc) == 8;
+    if (NT < 0 && int32_wide && (ORDER == kOrderDoubleTree || std::is_same<Op, OpProd>::value))
+        return 1;
+    return 2;
+}
+
 // ReduceScatter: index space [0, N*q), one store per element into the shard
 // that owns it.
-// Both reduction kernels state "at least one resident block" explicitly.
-// Measured on GB300 against the bare launch bound: ptxas then keeps more
-// loads in flight per thread, which lifts AllReduce by 0.5-1 % across the
-// board and the 64-rank tree from 0.78x to 1.06x the copy rate (the one
-// loss measured: bf16 RS at 32 ranks in the tree orders, 7.19 -> 6.54 TB/s).
 template <class T, class Op, int ORDER, int NT, int U>
-__global__ void __launch_bounds__(kThreads, 1) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kThreads, min_blocks<T, Op, ORDER, NT>()) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, true>(p);
 }
 
 // Fused AllReduce: index space [0, M), N stores per element (one, to the
 // root's buffer, for Reduce).
 template <class T, class Op, int ORDER, int NT, int U>
-__global__ void __launch_bounds__(kThreads, 1) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kThreads, min_blocks<T, Op, ORDER, NT>()) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, false>(p);
 }
 
@@ -710,16 +975,8 @@ constexpr int kGatherSlots = 8;
 template <int ES>
 __device__ __forceinline__ uint4 gather_load(const GatherParams& p, int s, long long i0) {
     using U = typename Bits<ES>::U;
-    constexpr int V = 16 / ES;
     const U* src = static_cast<const U*>(p.in[s]) + (i0 - (long long)s * p.q);
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) return ld16(src);
-    union {
-        U t[V];
-        uint4 u;
-    } w;
-#pragma unroll
-    for (int k = 0; k < V; ++k) w.t[k] = src[k];
-    return w.u;
+    return ld_aligned<ES>(src);
 }
 
 template <int ES>

@@ -24,7 +24,7 @@ cudaError_t launch_one(const ReduceParams& p, bool rs, cudaStream_t st) {
 // operands at a time.
 template <int N> constexpr int slots_for() { return N <= 4 ? 4 : (N <= 8 ? 2 : 1); }
 
-// Recursive halving and the (double) tree: N = 2, 4, ..., 64.
+// Recursive halving, and the tree orders at a power of two: N = 2, 4, ..., 64.
 template <class T, class Op, int ORDER>
 cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
     switch (p.n) {
@@ -35,6 +35,29 @@ cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
     case 32: return launch_one<T, Op, ORDER, 32, 1>(p, rs, st);
     case 64: return launch_one<T, Op, ORDER, 64, 1>(p, rs, st);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+// The tree orders take any N: compile-time N up to 8 and at the powers of
+// two; a run-time N inside a power-of-two envelope otherwise.  Floats: one
+// 64-rank envelope (a rank beyond N costs one uniform branch per tree
+// node).  Integers: the smallest envelope that holds N, its plain tree over
+// identity-padded ranks (a padded rank costs its combines, no load).
+template <class T, class Op, int ORDER>
+cudaError_t launch_tree(const ReduceParams& p, bool rs, cudaStream_t st) {
+    switch (p.n) {
+    case 3: return launch_one<T, Op, ORDER, 3, slots_for<3>()>(p, rs, st);
+    case 5: return launch_one<T, Op, ORDER, 5, slots_for<5>()>(p, rs, st);
+    case 6: return launch_one<T, Op, ORDER, 6, slots_for<6>()>(p, rs, st);
+    case 7: return launch_one<T, Op, ORDER, 7, slots_for<7>()>(p, rs, st);
+    default:
+        if (p.n < 2 || p.n > 64) return cudaErrorInvalidValue;
+        if (is_pow2(p.n)) return launch_pow2<T, Op, ORDER>(p, rs, st);
+        if constexpr (sizeof(typename Traits<T>::Acc) == 8) {
+            if (p.n < 16) return launch_one<T, Op, ORDER, -16, 1>(p, rs, st);
+            if (p.n < 32) return launch_one<T, Op, ORDER, -32, 1>(p, rs, st);
+        }
+        return launch_one<T, Op, ORDER, -64, 1>(p, rs, st);
     }
 }
 
@@ -59,14 +82,28 @@ cudaError_t launch_ring(const ReduceParams& p, bool rs, cudaStream_t st) {
     }
 }
 
-template <class T, class Op>
-cudaError_t launch_order(const ReduceParams& p, int order, bool rs, cudaStream_t st) {
-    // With one rank every order is the identity fold: a copy.
-    if (p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
-    if (order == kOrderRecursiveHalving)
+// The slice of the instances one translation unit holds (the build splits
+// them so the units compile in parallel): ring and recursive halving (and
+// every order at N = 1, a copy), the tree, or the double binary tree.
+enum { kGroupRingRh = 0, kGroupTree = 1, kGroupDoubleTree = 2 };
+
+__host__ __device__ constexpr int order_group(int order, int n) {
+    return (n == 1 || order == kOrderRing || order == kOrderRecursiveHalving)
+               ? kGroupRingRh
+               : (order == kOrderPairwiseTree ? kGroupTree : kGroupDoubleTree);
+}
+
+template <class T, class Op, int GROUP>
+cudaError_t launch_group(const ReduceParams& p, int order, bool rs, cudaStream_t st) {
+    if constexpr (GROUP == kGroupRingRh) {
+        // With one rank every order is the identity fold: a copy.
+        if (p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
         return launch_pow2<T, Op, kOrderRecursiveHalving>(p, rs, st);
-    if (order == kOrderDoubleTree) return launch_pow2<T, Op, kOrderDoubleTree>(p, rs, st);
-    return launch_pow2<T, Op, kOrderPairwiseTree>(p, rs, st);
+    } else if constexpr (GROUP == kGroupTree) {
+        return launch_tree<T, Op, kOrderPairwiseTree>(p, rs, st);
+    } else {
+        return launch_tree<T, Op, kOrderDoubleTree>(p, rs, st);
+    }
 }
 
 }  // namespace vc

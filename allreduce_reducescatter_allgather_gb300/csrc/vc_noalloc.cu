@@ -74,7 +74,7 @@ extern "C" vc_status_t vc_all_reduce_decomposed_noalloc(const void* const* sendb
     const int es = esize(dtype);
     if (es == 0 || op < VC_SUM || op > VC_AVG) return VC_ERR_INVALID_ARGUMENT;
     if (order < VC_ORDER_RING || order > VC_ORDER_DOUBLE_BINARY_TREE) return VC_ERR_INVALID_ARGUMENT;
-    if (order != VC_ORDER_RING && (nranks & (nranks - 1)) != 0) return VC_ERR_UNSUPPORTED;
+    if (order == VC_ORDER_RECURSIVE_HALVING && (nranks & (nranks - 1)) != 0) return VC_ERR_UNSUPPORTED;
     if (count == 0) return VC_SUCCESS;
     // the shards must fit the fixed scratch: N shards of q elements, each
     // rounded up to 256 bytes

@@ -1,18 +1,32 @@
-// From a run-time (element type, op) to the slice that holds its kernels.
-#include "vc_device.cuh"
+// From a run-time (element type, op, order) to the slice that holds its
+// kernels.
+#include "vc_launch.cuh"
 
 namespace vc {
 
-#define VC_DECLARE(ty)                                                                       \
-    cudaError_t launch_reduce_##ty##_sum(const ReduceParams&, int, bool, cudaStream_t);  \
-    cudaError_t launch_reduce_##ty##_prod(const ReduceParams&, int, bool, cudaStream_t); \
-    cudaError_t launch_reduce_##ty##_max(const ReduceParams&, int, bool, cudaStream_t);  \
-    cudaError_t launch_reduce_##ty##_min(const ReduceParams&, int, bool, cudaStream_t);
+#define VC_DECLARE_OP(ty, op)                                                                  \
+    cudaError_t launch_reduce_##ty##_##op##_g0(const ReduceParams&, int, bool, cudaStream_t); \
+    cudaError_t launch_reduce_##ty##_##op##_g1(const ReduceParams&, int, bool, cudaStream_t); \
+    cudaError_t launch_reduce_##ty##_##op##_g2(const ReduceParams&, int, bool, cudaStream_t); \
+    static cudaError_t launch_reduce_##ty##_##op(const ReduceParams& p, int order, bool rs,     \
+                                                 cudaStream_t st) {                            \
+        switch (order_group(order, p.n)) {                                                     \
+        case kGroupRingRh: return launch_reduce_##ty##_##op##_g0(p, order, rs, st);            \
+        case kGroupTree: return launch_reduce_##ty##_##op##_g1(p, order, rs, st);              \
+        default: return launch_reduce_##ty##_##op##_g2(p, order, rs, st);                      \
+        }                                                                                      \
+    }
+#define VC_DECLARE(ty)       \
+    VC_DECLARE_OP(ty, sum)   \
+    VC_DECLARE_OP(ty, prod)  \
+    VC_DECLARE_OP(ty, max)   \
+    VC_DECLARE_OP(ty, min)
 VC_DECLARE(i32)
 VC_DECLARE(i64)
 VC_DECLARE(f32)
 VC_DECLARE(bf16)
 #undef VC_DECLARE
+#undef VC_DECLARE_OP
 
 // op: 0 sum, 1 prod, 2 max, 3 min, 4 avg (the sum kernels with p.avg set)
 #define VC_DISPATCH(ty)                                                                         \

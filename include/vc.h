@@ -90,15 +90,19 @@ typedef enum {
  *    order, e.g. ((x0(+)x4)(+)(x2(+)x6))(+)((x1(+)x5)(+)(x3(+)x7)).  N must be
  *    a power of two (the page's hypercube condition).
  *  PAIRWISE_TREE: the binary tree of "通信与互联（01）" 六.1 (rank 0 the root
- *    with the single child N/2; rank r's level is its lowest set bit L and its
+ *    with a single child; rank r's level is its lowest set bit L and its
  *    parent is (r-L) | 2L; odd ranks are leaves).  An inner node's value is
  *    (left subtree (+) right subtree) (+) its own operand, the lower-ranked
- *    child on the left.  N must be a power of two.
- *  DOUBLE_BINARY_TREE: two complementary trees, each carrying half of the
- *    data ("通信与互联（01）" 六.3): the first ceil(count/2) elements in the
- *    PAIRWISE_TREE order (tree A), the others in tree B, which is tree A with
- *    every rank number shifted by one (node k is rank (k+1) mod N: root rank
- *    1, its child rank N/2 + 1, ...).  N must be a power of two. */
+ *    child on the left.  The page draws N = 8 only; for any N, a rank whose
+ *    parent label (r-L) | 2L is not a rank (>= N) hangs under r-L instead,
+ *    which keeps the tree binary with a single-child root and depth
+ *    ceil(log2 N).  Any N from 1 to VC_MAX_RANKS.
+ *  DOUBLE_BINARY_TREE: two trees, each carrying half of the data
+ *    ("通信与互联（01）" 六.3): the first ceil(count/2) elements in the
+ *    PAIRWISE_TREE order (tree A), the others in tree B, in which node k of
+ *    tree A is played by rank (k+1) mod N for even N (rank numbers shifted by
+ *    one: root rank 1, its child rank N/2 + 1, ...) and by rank N-1-k for odd
+ *    N (the mirror image).  Any N from 1 to VC_MAX_RANKS. */
 typedef enum {
     VC_ORDER_RING = 0,
     VC_ORDER_RECURSIVE_HALVING = 1,
@@ -112,7 +116,7 @@ typedef enum {
      * size, nranks outside [1, VC_MAX_RANKS], an unknown enum value, or a
      * count whose byte size exceeds 2^62 */
     VC_ERR_INVALID_ARGUMENT = 1,
-    /* RECURSIVE_HALVING or a tree order with nranks not a power of two */
+    /* RECURSIVE_HALVING with nranks not a power of two */
     VC_ERR_UNSUPPORTED = 2,
     /* an output range overlaps an input range or another output range (the
      * only overlap allowed is the in-place AllReduce, recvbufs[r] ==

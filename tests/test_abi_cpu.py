@@ -140,12 +140,12 @@ def test_count_zero_launches_nothing(vc):
 
 def test_power_of_two_orders(vc):
     """Recursive halving needs N = 2^k (the hypercube condition on the
-    "ReduceScatter" page); the tree order is read the same way."""
+    "ReduceScatter" page); the ring and both tree orders take any N."""
     for n in (3, 5, 6, 12, 63):
         s, r = fake(n, 1 << 40), fake(n, 2 << 40)
         assert rs(vc, s, r, n, 1000, order=RH) == UNSUPPORTED
-        assert ar(vc, s, r, n, 1000, order=TREE) == UNSUPPORTED
-        assert ar(vc, s, r, n, 1000, order=DTREE) == UNSUPPORTED
+        assert ar(vc, s, r, n, 1000, order=TREE) == CUDA
+        assert rs(vc, s, r, n, 1000, order=DTREE) == CUDA
         assert ar(vc, s, r, n, 1000, order=RING) == CUDA
     for n in (1, 2, 4, 8, 16, 32, 64):
         s, r = fake(n, 1 << 40), fake(n, 2 << 40)

@@ -42,7 +42,8 @@ def env():
 
 
 def orders_for(n):
-    return ORDERS if n & (n - 1) == 0 else ["ring"]
+    """Every order is defined for any N but recursive halving (N = 2^k)."""
+    return [o for o in ORDERS if n & (n - 1) == 0 or o != "recursive_halving"]
 
 
 def sentinel(dtype):
@@ -435,6 +436,53 @@ def test_edge_shapes(env, dtype, offset):
             xs = gen(dtype, n, M, seed=n * 1000 + M)
             res = run_all_paths(env, xs, dtype, op, order, offset=offset)
             check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M} off={offset}")
+
+
+TREE_N = [3, 5, 6, 7, 9, 12, 17, 24, 33, 48, 63]
+
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+@pytest.mark.parametrize("order", ["pairwise_tree", "double_binary_tree"])
+def test_trees_any_rank_count(env, dtype, order):
+    """Tree orders at rank counts that are not powers of two (compile-time
+    and run-time N, both envelopes): every path, every element, four ops, a
+    size that spans many blocks and ends in a ragged tail."""
+    k = 0
+    for n in TREE_N:
+        M = 40_000 + 13 * n + 1
+        op = SWEEP_OPS[k % 4]
+        k += 1
+        xs = gen(dtype, n, M, seed=5000 + n)
+        if op == "prod" and dtype in ("float32", "bfloat16"):
+            xs = gen_prod_floats(dtype, n, M)
+        res = run_all_paths(env, xs, dtype, op, order)
+        check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M}")
+
+
+@pytest.mark.parametrize("n", [6, 12, 48])
+def test_trees_any_rank_count_large_sampled(env, n):
+    """64 MiB per rank, N not a power of two: fused AR and RS in both tree
+    orders, sampled indices against the oracle; all AR outputs identical and
+    RS shard r == AR[rq : rq+q] on the device."""
+    vc, torch = env.vc, env.torch
+    M = 1 << 24
+    d = si.generate_device(torch, "float32", "normal", n, M, seed=90 + n, device=env.dev)
+    q = vc.vc_shard_count(M, n)
+    for order in ("pairwise_tree", "double_binary_tree"):
+        y = [torch.empty_like(t) for t in d]
+        z = [torch.empty(q, dtype=d[0].dtype, device=env.dev) for _ in range(n)]
+        vc.vc_all_reduce(d, y, op="sum", order=order)
+        vc.vc_reduce_scatter(d, z, op="sum", order=order)
+        torch.cuda.synchronize()
+        for r in range(n):
+            assert torch.equal(y[r], y[0])
+            lo, hi = r * q, min((r + 1) * q, M)
+            if lo < M:
+                assert torch.equal(z[r][:hi - lo], y[0][lo:hi])
+        _check_sampled(env, d, y[0], z, "float32", "sum", order, seed=n, K=1 << 16)
+        del y, z
+    del d
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("dtype", SWEEP_DTYPES)
