@@ -735,8 +735,10 @@ def run_sweep(args):
     JSON line per point with RS / AG / fused AR GB/s and their fraction of the
     measured copy peak (SUM, the order given by --order).  Inputs are made on
     the device; each kernel's time is the median of 5 single calls after 3
-    warm-ups, with the L2 flushed before each call where the data could
-    otherwise stay in it."""
+    warm-ups.  Before each call a write of twice the L2 evicts the last
+    call's data, and it keeps the GPU busy while the host issues the call:
+    the events then time the call on the device, launch latency included,
+    without the host's time to reach the launch."""
     import torch
 
     import allreduce_reducescatter_allgather_gb300 as vc
@@ -751,13 +753,12 @@ def run_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
 
-    def t_ms(fn, small, reps=5):
+    def t_ms(fn, reps=5):
         for _ in range(3):
             fn()
         times = []
         for _ in range(reps):
-            if small:
-                flush.zero_()
+            flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -767,7 +768,7 @@ def run_sweep(args):
         return sorted(times)[len(times) // 2]
 
     for n, nbytes in si.sweep_points():
-        if args.order != "ring" and n & (n - 1):
+        if args.order == "recursive_halving" and n & (n - 1):
             continue
         for dtype in ("float32", "bfloat16", "int32", "int64"):
             es = ESIZE[dtype]
@@ -781,15 +782,13 @@ def run_sweep(args):
             ag = vc.prepare_all_gather(z, d)  # AG writes over the inputs, after RS
             ar = vc.prepare_all_reduce(d, None, op=args.op, order=args.order)  # in place
             b = step_bytes(n, M, es)
-            small = 2 * n * nbytes < 4 * l2  # inputs + outputs could stay in L2
             line = {"sweep": "size_x_ranks", "n": n, "bytes_per_rank": nbytes, "dtype": dtype,
                     "op": args.op, "order": args.order, "peak": peak, "peak_kind": kind,
-                    "timing": "median of 5 single calls" + (", L2 flushed before each"
-                                                            if small else "")}
+                    "timing": "median of 5 single calls, each after an L2-evicting write"}
             for name, fn, key in (("reduce_scatter", rs, "reduce_scatter"),
                                   ("all_gather", ag, "all_gather"),
                                   ("all_reduce", ar, "fused_ar")):
-                ms = t_ms(lambda: fn(stream=stream), small)
+                ms = t_ms(lambda: fn(stream=stream))
                 g = b[key] / (ms / 1e3) / 1e9
                 line[name] = {"us": round(ms * 1e3, 2), "gbs": round(g, 1),
                               "frac": round(g / peak, 4)}
