@@ -681,3 +681,61 @@ def test_prepared_calls_replay_from_a_cuda_graph(env):
             assert_bits_equal(to_host(y[r], "float32"), oy[r], "float32", "graph AR")
             assert_bits_equal(to_host(z[r], "float32"), oz[r], "float32", "graph RS")
             assert_bits_equal(to_host(y2[r], "float32"), ot[r], "float32", "graph dec")
+
+
+# ------------------------------------------- the gather's early launch --
+
+@pytest.mark.parametrize("n,M", [(4, 4099), (8, 262_147), (4, 1 << 22), (12, 1_000_003)])
+def test_decomposed_back_to_back_matches_fused(env, n, M):
+    """The AllGather of a decomposed AllReduce may be scheduled while the
+    ReduceScatter before it drains; it must still see every shard element
+    that ReduceScatter wrote.  Many decomposed calls back to back on fresh
+    inputs (each input written by a torch kernel right before), each
+    compared on the device with the fused AllReduce of the same inputs."""
+    vc, torch = env.vc, env.torch
+    q = vc.vc_shard_count(M, n)
+    base = [torch.randn(M, device=env.dev) for _ in range(n)]
+    d = [torch.empty_like(t) for t in base]
+    y = [torch.empty_like(t) for t in base]
+    y2 = [torch.empty_like(t) for t in base]
+    sh = [torch.empty(q, device=env.dev) for _ in range(n)]
+    ar = vc.prepare_all_reduce(d, y, order="ring")
+    dec = vc.prepare_all_reduce_decomposed(d, sh, y2, order="ring")
+    bad = torch.zeros((), dtype=torch.int64, device=env.dev)
+    for it in range(40):
+        for t, b in zip(d, base):
+            torch.mul(b, float(it + 1), out=t)
+        dec()
+        ar()
+        for r in range(n):
+            bad += (y2[r] != y[0]).sum()
+        bad += (y[n - 1] != y[0]).sum()
+    torch.cuda.synchronize()
+    assert int(bad) == 0
+    # and the last call against the oracle
+    xs = [to_host(t, "float32") for t in d]
+    oy = oracle.all_reduce(xs, "float32", "sum", "ring")
+    assert_bits_equal(to_host(y2[0], "float32"), oy[0], "float32", "last decomposed")
+
+
+def test_all_gather_right_after_a_kernel_that_writes_the_shards(env):
+    """AllGather launched directly after a torch kernel that produces the
+    shards (a kernel that never signals an early start): it must wait for
+    that kernel's writes."""
+    vc, torch = env.vc, env.torch
+    n, M = 8, 1 << 21
+    q = vc.vc_shard_count(M, n)
+    src = [torch.randn(q, device=env.dev) for _ in range(n)]
+    z = [torch.empty(q, device=env.dev) for _ in range(n)]
+    out = [torch.empty(M, device=env.dev) for _ in range(n)]
+    ag = vc.prepare_all_gather(z, out)
+    bad = torch.zeros((), dtype=torch.int64, device=env.dev)
+    for it in range(40):
+        for t, s in zip(z, src):
+            torch.add(s, float(it), out=t)
+        ag()
+        want = torch.cat(z)[:M]
+        for r in range(n):
+            bad += (out[r] != want).sum()
+    torch.cuda.synchronize()
+    assert int(bad) == 0
