@@ -739,3 +739,38 @@ def test_all_gather_right_after_a_kernel_that_writes_the_shards(env):
             bad += (out[r] != want).sum()
     torch.cuda.synchronize()
     assert int(bad) == 0
+
+
+# -------------------------------------------------------- maximum sizes --
+
+@pytest.mark.parametrize("n", [3, 9])
+def test_more_than_2_31_elements_per_rank(env, n):
+    """Element indices past 2^31 (bf16, 2^31 + 13 elements = 4 GiB per rank;
+    three ranks take a compile-time ring, nine the run-time-N ring; shards
+    off the 16-byte grid): fused AR and RS, sampled indices against the
+    oracle (every chunk boundary and the last elements included), all AR
+    outputs identical, and RS shard r == AR[rq : rq+q]."""
+    vc, torch = env.vc, env.torch
+    M = (1 << 31) + 13
+    d = []
+    for r in range(n):
+        g = torch.Generator(device=env.dev)
+        g.manual_seed(700 + r)
+        d.append(torch.empty(M, dtype=torch.bfloat16, device=env.dev))
+        # in 2^28-element slices, to keep the fp32 temporary small
+        for lo in range(0, M, 1 << 28):
+            hi = min(M, lo + (1 << 28))
+            d[r][lo:hi] = torch.randn(hi - lo, generator=g, device=env.dev)
+    q = vc.vc_shard_count(M, n)
+    y = [torch.empty_like(t) for t in d]
+    z = [torch.empty(q, dtype=torch.bfloat16, device=env.dev) for _ in range(n)]
+    vc.vc_all_reduce(d, y, op="sum", order="ring")
+    vc.vc_reduce_scatter(d, z, op="sum", order="ring")
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert torch.equal(y[r], y[0])
+        lo, hi = r * q, min((r + 1) * q, M)
+        assert torch.equal(z[r][:hi - lo], y[0][lo:hi])
+    _check_sampled(env, d, y[0], z, "bfloat16", "sum", "ring", K=1 << 16, seed=31)
+    del d, y, z
+    torch.cuda.empty_cache()
