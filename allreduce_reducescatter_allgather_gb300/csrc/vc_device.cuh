@@ -5,11 +5,13 @@
 // a thread owns a 16-byte vector of consecutive indices, loads it from each
 // of the N rank buffers, folds the N vectors lane by lane in the order's fixed
 // tree, and stores the result (AllReduce: to all N outputs; ReduceScatter: to
-// the shard that owns the index).  Nothing waits on anything: no barrier, no
-// flag, no inter-block traffic.  The work is bound by HBM bandwidth, so the
-// design is about keeping many 16-byte loads in flight (groups of up to 8
-// independent loads per thread, a grid of whole waves of resident blocks) and
-// about never re-reading a byte.
+// the shard that owns the index).  No block waits on another: no flag, no
+// inter-block traffic.  (The one barrier is a block's own __syncthreads after
+// it copies the pointer table to shared memory; the one wait is the
+// AllGather's grid dependency on the kernel before it.)  The work is bound by
+// HBM bandwidth, so the design is about keeping many 16-byte loads in flight
+// (up to 16 independent loads per thread, many more blocks than are
+// resident) and about never re-reading a byte.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -819,11 +821,15 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
 // range (each warp access is 512 contiguous bytes).  When all U vectors sit
 // inside one chunk and inside the data on aligned bases (nearly always), the
 // thread issues every load before it folds or stores anything:
-//  - N <= 8 (NT > 0): the N x U vectors (at most 16) are loaded into
-//    registers in rank order, with constant rank indices, then folded slot by
-//    slot in the order's tree (the ring picks its rotation by the chunk);
-//  - otherwise (U = 1): the fold streams its operands in groups of kGroup;
-//    the ring with run-time N reads its rotated pointers from shared memory.
+//  - compile-time N <= 8 (0 < NT <= 8): the N x U vectors (at most 16) are
+//    loaded into registers in rank order, with constant rank indices, then
+//    folded slot by slot in the order's tree (the ring picks its rotation
+//    by the chunk);
+//  - otherwise (U = 1): the fold streams its operands in groups of kGroup.
+//    The ring beyond 8 ranks reads its pointers from a shared-memory copy
+//    of the table (doubled when N is a run-time value, so a rotation never
+//    wraps), and so do the trees with a run-time N (tree B computes its
+//    rank indices).
 // Anything else goes slot by slot through reduce_slot.
 template <class T, class Op, int ORDER, int NT, int U, bool RS>
 __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
@@ -1043,7 +1049,8 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
     }
 }
 
-// Launchers, one translation unit per element type (vc_reduce_<type>.cu).
+// Launchers by element type (vc_reduce_dispatch.cu, which picks the slice of
+// vc_reduce_inst.cu that holds the op and order).
 cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int order, bool rs, cudaStream_t st);
 cudaError_t launch_reduce_i64(const ReduceParams& p, int op, int order, bool rs, cudaStream_t st);
 cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int order, bool rs, cudaStream_t st);

@@ -1,5 +1,6 @@
 // Dispatch from a run-time (order, N) to a kernel instance.  Included by
-// vc_reduce_inst.cu, which the build compiles once per (element type, op).
+// vc_reduce_inst.cu, which the build compiles once per (element type, op,
+// order group), and by vc_reduce_dispatch.cu for order_group().
 #pragma once
 
 #include "vc_device.cuh"
