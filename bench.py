@@ -65,10 +65,21 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines: a comment edit does not
+    change the kernels, so it does not void a recorded ncu figure."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def source_digest() -> str:
+    """Digest of the CUDA sources' code (comments and blank lines removed)."""
     h = hashlib.sha256()
     for f in sorted((ROOT / "allreduce_reducescatter_allgather_gb300" / "csrc").glob("*")):
-        h.update(f.read_bytes())
+        h.update(f.name.encode())
+        h.update(_code_only(f.read_text()).encode())
     return h.hexdigest()[:16]
 
 
