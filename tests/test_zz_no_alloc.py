@@ -40,7 +40,9 @@ CASES = [("float32", 8, 1_000_003, "sum", "ring"),
          ("bfloat16", 8, 2_000_001, "avg", "pairwise_tree"),
          ("int64", 4, 777_777, "prod", "ring"),
          ("int32", 64, 65_537, "max", "ring"),
-         ("float32", 3, 17, "min", "ring")]
+         ("float32", 3, 17, "min", "ring"),
+         ("float32", 12, 300_007, "sum", "double_binary_tree"),
+         ("int32", 5, 100_003, "sum", "pairwise_tree")]
 
 
 def _inputs(dtype, n, M, seed):
