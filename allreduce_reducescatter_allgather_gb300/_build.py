@@ -24,14 +24,16 @@ SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu", "vc_copy.cu"]
 HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
 # vc_reduce_inst.cu compiled once per (element type, op, order group):
 # (object, -D flags).  Groups: 0 ring + recursive halving, 1 tree, 2 double
-# binary tree.
+# binary tree.  The integer types have group 0 only (ring): their results
+# do not depend on the order, so every order runs on the ring's kernels.
 INSTANCE_SOURCE = "vc_reduce_inst.cu"
 _TYPES = {"i32": "int32_t", "i64": "long long", "f32": "float", "bf16": "__nv_bfloat16"}
 _OPS = {"sum": "OpSum", "prod": "OpProd", "max": "OpMax", "min": "OpMin"}
 _GROUPS = (0, 1, 2)
 INSTANCES = [(f"vc_reduce_{t}_{o}_g{g}", [f"-DVC_T={ct}", f"-DVC_OP={op}", f"-DVC_GROUP={g}",
                                           f"-DVC_FN=launch_reduce_{t}_{o}_g{g}"])
-             for t, ct in _TYPES.items() for o, op in _OPS.items() for g in _GROUPS]
+             for t, ct in _TYPES.items() for o, op in _OPS.items()
+             for g in (_GROUPS if t in ("f32", "bf16") else (0,))]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

@@ -292,7 +292,6 @@ __device__ __forceinline__ long long avg_div(long long s, int n) { return s / (l
 // The 16-byte vector at element offset i0 of rank r.
 template <class T> struct VecLoader {
     using A = typename Traits<T>::Acc;
-    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const ReduceParams& p;
@@ -311,7 +310,6 @@ template <class T> struct VecLoader {
 // from M to N*q.
 template <class T, class Op> struct ScalarLoader {
     using A = typename Traits<T>::Acc;
-    using Elem = T;
     static constexpr int W = 1;
     using Raw = A;
     const ReduceParams& p;
@@ -331,7 +329,6 @@ template <class T, class Op> struct ScalarLoader {
 // whose rank index is only known at run time).
 template <class T> struct SharedTableLoader {
     using A = typename Traits<T>::Acc;
-    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const void* const* table;
@@ -350,7 +347,6 @@ template <class T> struct SharedTableLoader {
 // the thread's slot u.
 template <class T, int NR, int U> struct PreLoader {
     using A = typename Traits<T>::Acc;
-    using Elem = T;
     static constexpr int W = Traits<T>::V;
     using Raw = uint4;
     const uint4 (&buf)[NR][U];
@@ -376,7 +372,6 @@ __host__ __device__ constexpr int tree_b_rank(int k, int n) {
 // compile-time constant.
 template <class L, int N> struct TreeBStatic {
     using A = typename L::A;
-    using Elem = typename L::Elem;
     static constexpr int W = L::W;
     using Raw = typename L::Raw;
     const L& l;
@@ -387,41 +382,11 @@ template <class L, int N> struct TreeBStatic {
 // The second tree with a run-time N (the rank index is computed).
 template <class L> struct TreeBRuntime {
     using A = typename L::A;
-    using Elem = typename L::Elem;
     static constexpr int W = L::W;
     using Raw = typename L::Raw;
     const L& l;
     int n;
     __device__ __forceinline__ Raw raw(int k) const { return l.raw(tree_b_rank(k, n)); }
-    __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
-};
-
-// Ranks n .. of a power-of-two envelope, holding the op's identity e (no
-// load).  For integers x (+) e = x exactly for every op, so the envelope's
-// tree over the padded ranks gives the same value, bit for bit, as the tree
-// over n ranks in which a missing rank passes its one subtree through: a
-// node with a missing right subtree computes (l (+) e) (+) own = l (+) own,
-// and a missing node (l (+) e) (+) e = l.  (Floats are not padded this way:
-// -0 (+) +0 is +0.)  The padded tree has no branches, so the compiler can
-// schedule every load early.
-template <class L, class Op> struct IdentityPadded {
-    using A = typename L::A;
-    static constexpr int W = L::W;
-    using Raw = typename L::Raw;
-    using Elem = typename L::Elem;
-    const L& l;
-    int n;
-    __device__ __forceinline__ static Raw identity() {
-        if constexpr (W == 1) {
-            return Identity<Elem, Op>::get();
-        } else {
-            Vec<A, W> e;
-#pragma unroll
-            for (int k = 0; k < W; ++k) e.x[k] = Identity<Elem, Op>::get();
-            return pack(e, (Elem*)nullptr);
-        }
-    }
-    __device__ __forceinline__ Raw raw(int k) const { return k < n ? l.raw(k) : identity(); }
     __device__ __forceinline__ Vec<A, W> cvt(const Raw& r) const { return l.cvt(r); }
 };
 
@@ -676,12 +641,7 @@ __host__ __device__ constexpr int pow2_ceil(int n) { return n <= 1 ? 1 : 2 * pow
 // takes the plain tree), NT < 0 a run-time n inside the envelope -NT.
 template <class Op, int NT, class Ld>
 __device__ __forceinline__ VecOf<Ld> fold_any_tree(const Ld& ld, int n) {
-    if constexpr (NT < 0 && sizeof(typename Ld::A) == 8) {
-        // integers: the plain tree of the envelope over identity-padded ranks
-        // (exact, see IdentityPadded)
-        IdentityPadded<Ld, Op> padded{ld, n};
-        return fold_tree<Op, -NT>(padded);
-    } else if constexpr (NT < 0) {
+    if constexpr (NT < 0) {
         return fold_tree_n<Op, -NT>(ld, n);
     } else if constexpr (is_pow2(NT)) {
         return fold_tree<Op, NT>(ld);
@@ -936,31 +896,24 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
 // 1.06x the copy rate (the one loss measured: bf16 RS at 32 ranks in the
 // tree orders, 7.19 -> 6.54 TB/s).  Run-time N (folds that stream 16
 // operands at a time): two, so that a second block hides the first one's
-// load latency.  Measured: the ring at N = 12 from 0.81x to 0.96x (bf16
-// 0.67x to 0.82x); the padded int64 tree at N = 63 from 0.81x to 0.98x.
-// The exceptions keep one: int32 trees with a run-time N in the double
-// binary tree (at 128 registers it spills and fell from 0.72x to 0.62x) or
-// with PROD (64-bit products: hundreds of bytes of spills at 128).
-template <class T, class Op, int ORDER, int NT>
+// load latency; measured, the ring at N = 12 went from 0.81x to 0.96x (bf16
+// 0.67x to 0.82x).
+template <int NT>
 constexpr int min_blocks() {
-    if (NT > 0) return 1;
-    constexpr bool int32_wide = sizeof(T) == 4 && sizeof(typename Traits<T>::Acc) == 8;
-    if (NT < 0 && int32_wide && (ORDER == kOrderDoubleTree || std::is_same<Op, OpProd>::value))
-        return 1;
-    return 2;
+    return NT > 0 ? 1 : 2;
 }
 
 // ReduceScatter: index space [0, N*q), one store per element into the shard
 // that owns it.
 template <class T, class Op, int ORDER, int NT, int U>
-__global__ void __launch_bounds__(kThreads, min_blocks<T, Op, ORDER, NT>()) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kThreads, min_blocks<NT>()) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, true>(p);
 }
 
 // Fused AllReduce: index space [0, M), N stores per element (one, to the
 // root's buffer, for Reduce).
 template <class T, class Op, int ORDER, int NT, int U>
-__global__ void __launch_bounds__(kThreads, min_blocks<T, Op, ORDER, NT>()) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kThreads, min_blocks<NT>()) vc_ar_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, false>(p);
 }
 

@@ -40,12 +40,13 @@ cudaError_t launch_pow2(const ReduceParams& p, bool rs, cudaStream_t st) {
 }
 
 // The tree orders take any N: compile-time N up to 8 and at the powers of
-// two; a run-time N inside a power-of-two envelope otherwise.  Floats: one
-// 64-rank envelope (a rank beyond N costs one uniform branch per tree
-// node).  Integers: the smallest envelope that holds N, its plain tree over
-// identity-padded ranks (a padded rank costs its combines, no load).
+// two; a run-time N inside the 64-rank envelope otherwise (a rank beyond N
+// costs one uniform branch per tree node).  Floats only: the integer types
+// run every order on the ring's kernels (vc_reduce_dispatch.cu).
 template <class T, class Op, int ORDER>
 cudaError_t launch_tree(const ReduceParams& p, bool rs, cudaStream_t st) {
+    static_assert(std::is_same<typename Traits<T>::Acc, float>::value,
+                  "tree instances exist for the float types only");
     switch (p.n) {
     case 3: return launch_one<T, Op, ORDER, 3, slots_for<3>()>(p, rs, st);
     case 5: return launch_one<T, Op, ORDER, 5, slots_for<5>()>(p, rs, st);
@@ -54,10 +55,6 @@ cudaError_t launch_tree(const ReduceParams& p, bool rs, cudaStream_t st) {
     default:
         if (p.n < 2 || p.n > 64) return cudaErrorInvalidValue;
         if (is_pow2(p.n)) return launch_pow2<T, Op, ORDER>(p, rs, st);
-        if constexpr (sizeof(typename Traits<T>::Acc) == 8) {
-            if (p.n < 16) return launch_one<T, Op, ORDER, -16, 1>(p, rs, st);
-            if (p.n < 32) return launch_one<T, Op, ORDER, -32, 1>(p, rs, st);
-        }
         return launch_one<T, Op, ORDER, -64, 1>(p, rs, st);
     }
 }
@@ -97,9 +94,12 @@ __host__ __device__ constexpr int order_group(int order, int n) {
 template <class T, class Op, int GROUP>
 cudaError_t launch_group(const ReduceParams& p, int order, bool rs, cudaStream_t st) {
     if constexpr (GROUP == kGroupRingRh) {
-        // With one rank every order is the identity fold: a copy.
-        if (p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
-        return launch_pow2<T, Op, kOrderRecursiveHalving>(p, rs, st);
+        // With one rank every order is the identity fold: a copy.  Integers
+        // give the same bits in every order, so they only have the ring.
+        constexpr bool kInt = !std::is_same<typename Traits<T>::Acc, float>::value;
+        if (kInt || p.n == 1 || order == kOrderRing) return launch_ring<T, Op>(p, rs, st);
+        if constexpr (!kInt) return launch_pow2<T, Op, kOrderRecursiveHalving>(p, rs, st);
+        return cudaErrorInvalidValue;
     } else if constexpr (GROUP == kGroupTree) {
         return launch_tree<T, Op, kOrderPairwiseTree>(p, rs, st);
     } else {

@@ -50,7 +50,9 @@ extern "C" {
 #define VC_MAX_RANKS 64
 
 /* Element types.  Integers accumulate in 64 bits and wrap modulo 2^64
- * (int32 results are the low 32 bits); float32 accumulates in float32;
+ * (int32 results are the low 32 bits), so an integer result is the same in
+ * every reduction order (every order is computed with the ring's kernels);
+ * float32 accumulates in float32;
  * bfloat16 is widened exactly to float32, accumulated in float32 and rounded
  * once to nearest-even at the store.  (The pages fix no accumulator for
  * bf16; they note that float reduction is not associative, 条件五.) */
