@@ -29,7 +29,14 @@ MAX_RANKS = 64
 # Every function the header declares (checked by the tests against vc.h).
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
            "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles",
-           "vc_all_reduce_decomposed_noalloc", "vc_status_string")
+           "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan", "vc_all_reduce_bucket",
+           "vc_status_string")
+
+
+class BucketTile(ctypes.Structure):
+    """vc_bucket_tile_t."""
+    _fields_ = [("bucket_offset", ctypes.c_longlong), ("tensor_offset", ctypes.c_longlong),
+                ("count", ctypes.c_longlong), ("tensor", ctypes.c_int), ("flags", ctypes.c_int)]
 
 
 class VcError(RuntimeError):
@@ -63,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.vc_reduce.argtypes = [vpp, vp, i32, sz, i32, i32, i32, vp]
         L.vc_broadcast.argtypes = [vp, vpp, i32, sz, i32, vp]
         L.vc_copy_tiles.argtypes = [vp, i32, vp]
+        L.vc_bucket_plan.argtypes = [vpp, vpp, ctypes.POINTER(sz), i32, i32, i32, i32,
+                                     ctypes.POINTER(BucketTile), i32, ctypes.POINTER(i32),
+                                     ctypes.POINTER(sz)]
+        L.vc_all_reduce_bucket.argtypes = [vp, i32, vp, vp, i32, sz, i32, i32, vp]
+        L.vc_bucket_plan.restype = i32
+        L.vc_all_reduce_bucket.restype = i32
         for f in ("vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
                   "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles"):
             getattr(L, f).restype = i32
@@ -365,3 +378,68 @@ def vc_all_reduce_decomposed_noalloc(sendbufs, recvbufs=None, op: str = "sum",
     fn.restype = ctypes.c_int
     check_status(fn(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order],
                     _stream(stream, dev)))
+
+
+# ------------------------------------------------------------ fused buckets --
+
+class BucketAllReduce:
+    """The AllReduce of a gradient bucket whose tensors stay where they are
+    (vc_bucket_plan + vc_all_reduce_bucket): tensors[r][k] is tensor k of
+    rank r, out[r][k] its output (None: in place).  The bucket holds the
+    tensors in the order given, each on a 16-byte boundary; every element
+    gets the bits the ring-order AllReduce of that bucket gives it.  Planned
+    once (pointer checks, aliasing, tiles); each call is one launch.  The
+    plan keeps the tensors' addresses: make a new one if they change."""
+
+    def __init__(self, tensors, out=None, order: str = "ring"):
+        import torch
+        n = len(tensors)
+        if n < 1 or n > MAX_RANKS:
+            raise ValueError(f"1 <= ranks <= {MAX_RANKS}")
+        out = tensors if out is None else out
+        nt = len(tensors[0])
+        if any(len(t) != nt for t in tensors) or len(out) != n or any(len(o) != nt for o in out):
+            raise ValueError("every rank needs the same number of tensors, inputs and outputs")
+        if nt == 0:
+            raise ValueError("a bucket needs at least one tensor")
+        dt = _dtype_name(tensors[0][0])
+        dev = tensors[0][0].device
+        counts = [tensors[0][k].numel() for k in range(nt)]
+        for r in range(n):
+            for k in range(nt):
+                for name, t in (("tensors", tensors[r][k]), ("out", out[r][k])):
+                    if not (t.is_cuda and t.device == dev and t.is_contiguous()
+                            and _dtype_name(t) == dt and t.numel() == counts[k]):
+                        raise ValueError(f"{name}[{r}][{k}] does not match tensor {k} of rank 0 "
+                                         f"(device, dtype, contiguity, numel)")
+        L = lib()
+        ins = [tensors[r][k].data_ptr() for k in range(nt) for r in range(n)]
+        outs = [out[r][k].data_ptr() for k in range(nt) for r in range(n)]
+        in_tab = (ctypes.c_void_p * len(ins))(*ins)
+        out_tab = (ctypes.c_void_p * len(outs))(*outs)
+        cnt = (ctypes.c_size_t * nt)(*counts)
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        ntiles, bucket_count = ctypes.c_int(0), ctypes.c_size_t(0)
+        args = (ctypes.cast(in_tab, vpp), ctypes.cast(out_tab, vpp), cnt, nt, n, DTYPES[dt],
+                ORDERS[order])
+        check_status(L.vc_bucket_plan(*args, None, 0, ctypes.byref(ntiles),
+                                      ctypes.byref(bucket_count)))
+        tiles = (BucketTile * max(1, ntiles.value))()
+        check_status(L.vc_bucket_plan(*args, tiles, ntiles.value, ctypes.byref(ntiles),
+                                      ctypes.byref(bucket_count)))
+        self.ntiles, self.bucket_count, self.nranks, self.dtype = (ntiles.value,
+                                                                  bucket_count.value, n, dt)
+        self.device = dev
+        raw = bytes(memoryview(tiles).cast("B"))[:ctypes.sizeof(BucketTile) * ntiles.value]
+        self.tiles = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(dev)
+        self.in_ptrs = torch.tensor(ins, dtype=torch.int64).to(dev)
+        self.out_ptrs = torch.tensor(outs, dtype=torch.int64).to(dev)
+        self._keep = (tensors, out)
+        self.host_tiles = tiles
+
+    def __call__(self, op: str = "sum", stream=None):
+        check_status(lib().vc_all_reduce_bucket(
+            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
+            ctypes.c_void_p(self.in_ptrs.data_ptr()), ctypes.c_void_p(self.out_ptrs.data_ptr()),
+            self.nranks, self.bucket_count, DTYPES[self.dtype], OPS[op],
+            _stream(stream, self.device)))

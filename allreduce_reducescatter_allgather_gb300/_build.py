@@ -20,8 +20,8 @@ BUILD = PKG / "_build"
 LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "libvc.so"
 
-SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu", "vc_copy.cu"]
-HEADERS = ["vc_device.cuh", "vc_launch.cuh"]
+SOURCES = ["vc_api.cu", "vc_reduce_dispatch.cu", "vc_noalloc.cu", "vc_copy.cu", "vc_bucket.cu"]
+HEADERS = ["vc_device.cuh", "vc_launch.cuh", "vc_bucket_kernel.cuh"]
 # vc_reduce_inst.cu compiled once per (element type, op, order group):
 # (object, -D flags).  Groups: 0 ring + recursive halving, 1 tree, 2 double
 # binary tree.  The integer types have group 0 only (ring): their results
@@ -34,6 +34,10 @@ INSTANCES = [(f"vc_reduce_{t}_{o}_g{g}", [f"-DVC_T={ct}", f"-DVC_OP={op}", f"-DV
                                           f"-DVC_FN=launch_reduce_{t}_{o}_g{g}"])
              for t, ct in _TYPES.items() for o, op in _OPS.items()
              for g in (_GROUPS if t in ("f32", "bf16") else (0,))]
+# vc_bucket_inst.cu (the fused bucket AllReduce kernels) once per element type
+BUCKET_SOURCE = "vc_bucket_inst.cu"
+BUCKET_INSTANCES = [(f"vc_bucket_{t}", [f"-DVC_T={ct}", f"-DVC_FN=launch_bucket_{t}"])
+                    for t, ct in _TYPES.items()]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
@@ -54,8 +58,8 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES + HEADERS + [INSTANCE_SOURCE]] + [INCLUDE / "vc.h",
-                                                                       Path(__file__)]
+    deps = [CSRC / s for s in SOURCES + HEADERS + [INSTANCE_SOURCE, BUCKET_SOURCE]] + [
+        INCLUDE / "vc.h", Path(__file__)]
     return any(d.stat().st_mtime > t for d in deps)
 
 
@@ -80,9 +84,11 @@ def build_library(force: bool = False, jobs: int | None = None) -> Path:
 
     jobs_list = [(Path(s).stem, s, []) for s in SOURCES]
     jobs_list += [(stem, INSTANCE_SOURCE, defs) for stem, defs in INSTANCES]
-    # the largest slices first (double tree, tree, ring), so the pool
-    # finishes together
-    jobs_list.sort(key=lambda j: -int(j[0][-1]) if j[1] == INSTANCE_SOURCE else 1)
+    jobs_list += [(stem, BUCKET_SOURCE, defs) for stem, defs in BUCKET_INSTANCES]
+    # the largest slices first (double tree, tree, ring and bucket), so the
+    # pool finishes together
+    jobs_list.sort(key=lambda j: -int(j[0][-1]) if j[1] == INSTANCE_SOURCE
+                   else (0 if j[1] == BUCKET_SOURCE else 1))
     jobs = jobs or max(1, os.cpu_count() or 4)
     with ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(compile_one, jobs_list))

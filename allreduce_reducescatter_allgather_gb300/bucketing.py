@@ -9,12 +9,17 @@ runs and sends it when it is full.  Its caps are 25 MiB per bucket
 saving is one kernel launch per bucket instead of one per tensor, and a
 bucket large enough to run at the HBM rate.
 
-Two ways to feed a bucket:
+Three ways to feed a bucket:
  - views (no copy): every gradient tensor is a view into its rank's flat
    bucket buffer (what DDP calls gradients as bucket views); the AllReduce
    runs in place on the buckets and the views hold the results;
- - packing: tensors that live elsewhere are copied into the buckets and back
-   with vc_copy_tiles, one launch per direction per bucket.
+ - fused: tensors that live elsewhere are reduced where they are, one launch
+   per bucket (vc_bucket_plan + vc_all_reduce_bucket), with the bits the
+   bucket's AllReduce gives them: integers in every order, floats in ring
+   order;
+ - packing: tensors are copied into the buckets and back with
+   vc_copy_tiles around the bucket's AllReduce, three launches per bucket
+   (any order).
 
 Assignment rule (the pages give only the caps; this is the plain reading):
 tensors are taken in reverse order, the order backward produces their
@@ -64,6 +69,7 @@ class _Bucket:
     pack_tiles: object = None    # device table for vc_copy_tiles (tensors -> bucket)
     unpack_tiles: object = None  # (bucket -> tensors)
     ntiles: int = 0
+    fused: object = None         # BucketAllReduce over the bound tensors, in place
 
 
 class GradientBuckets:
@@ -155,14 +161,34 @@ class GradientBuckets:
             b.pack_tiles = torch.tensor(pack, dtype=torch.int64).to(self.device)
             b.unpack_tiles = torch.tensor(unpack, dtype=torch.int64).to(self.device)
             b.ntiles = len(pack)
+            # the fused call lays the bucket out the same way: its tensors in
+            # fill order, each on a 16-byte boundary
+            b.fused = _binding.BucketAllReduce(
+                [[grads[r][t] for t in b.tensors] for r in range(self.nranks)])
+            assert b.fused.bucket_count == b.count or not any(self.numels[t] for t in b.tensors)
         self.bound = grads
 
-    def all_reduce_tensors(self, op: str = "sum", order: str = "ring", stream=None):
-        """For the bound tensors: per bucket, pack (one launch), AllReduce in
-        place (one launch), unpack (one launch)."""
+    def fused_supported(self, order: str) -> bool:
+        """Whether all_reduce_tensors(fused=True) takes one launch per bucket
+        for this order: always for integers (order-free), the ring for floats."""
+        return order == "ring" or self.dtype not in (self.torch.float32, self.torch.bfloat16)
+
+    def all_reduce_tensors(self, op: str = "sum", order: str = "ring", stream=None,
+                           fused: bool = True):
+        """For the bound tensors, in place.  fused (when the order allows it,
+        see fused_supported): one launch per bucket that reduces the tensors
+        where they are.  Otherwise, per bucket: pack (one launch), AllReduce
+        in place (one launch), unpack (one launch).  Both give the bits of
+        the bucket views path."""
         torch = self.torch
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
+        if fused and self.fused_supported(order):
+            if order == "recursive_halving" and self.nranks & (self.nranks - 1):
+                raise ValueError("recursive halving needs a power-of-two rank count")
+            for b in self.buckets:
+                b.fused(op=op, stream=stream)
+            return
         import ctypes
         L = _binding.lib()
         s = ctypes.c_void_p(stream.cuda_stream)

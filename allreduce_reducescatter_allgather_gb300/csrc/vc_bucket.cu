@@ -1,0 +1,188 @@
+// vc_bucket_plan / vc_all_reduce_bucket: the AllReduce of a gradient bucket
+// whose tensors stay where they are.
+//
+// A DDP bucket ("通信与互联（01）" 三.1 and 九.1) is a flat buffer per rank
+// into which many gradient tensors are packed, so one AllReduce replaces
+// many small ones.  When the tensors live elsewhere, pack -> AllReduce ->
+// unpack reads and writes every byte three times.  Here one kernel reads
+// each tensor element from the N ranks' tensors, folds it in ring order with
+// the ring chunk of its place in the bucket, and writes the result back to
+// the N ranks' output tensors: the bits of the packed path, a third of its
+// traffic, one launch.
+//
+// The host plan (vc_bucket_plan) lays the tensors out as the bucket would
+// hold them and cuts them into tiles that never cross a ring chunk, so a
+// tile's chunk is a constant.  The kernel takes tiles in a grid-stride loop;
+// for each, the block copies the tensor's N input pointers (twice, so the
+// ring's rotation never wraps) and N output pointers into shared memory.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "vc.h"
+#include "vc_bucket_kernel.cuh"
+
+namespace vc {
+namespace {
+
+int esize(vc_dtype_t dt) {
+    switch (dt) {
+    case VC_INT32: return 4;
+    case VC_INT64: return 8;
+    case VC_FLOAT32: return 4;
+    case VC_BFLOAT16: return 2;
+    default: return 0;
+    }
+}
+
+bool launch_failure_injected() {
+    const char* v = getenv("VC_TEST_FAIL_LAUNCH");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+struct Span {
+    uintptr_t lo, hi;
+    int tensor, rank;
+};
+
+// Outputs must not overlap each other; an input may overlap only its own
+// output, exactly (in place).
+vc_status_t check_bucket_alias(const std::vector<Span>& ins, std::vector<Span> outs) {
+    std::sort(outs.begin(), outs.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+    for (size_t k = 0; k + 1 < outs.size(); ++k)
+        if (outs[k].hi > outs[k + 1].lo) return VC_ERR_ALIAS;
+    for (const Span& s : ins) {
+        // first output that ends after the input starts
+        size_t lo = 0, hi = outs.size();
+        while (lo < hi) {
+            const size_t mid = (lo + hi) / 2;
+            if (outs[mid].hi <= s.lo) lo = mid + 1; else hi = mid;
+        }
+        for (size_t k = lo; k < outs.size() && outs[k].lo < s.hi; ++k) {
+            const Span& o = outs[k];
+            const bool in_place = o.tensor == s.tensor && o.rank == s.rank && o.lo == s.lo &&
+                                  o.hi == s.hi;
+            if (!in_place) return VC_ERR_ALIAS;
+        }
+    }
+    return VC_SUCCESS;
+}
+
+}  // namespace
+}  // namespace vc
+
+using namespace vc;
+
+extern "C" vc_status_t vc_bucket_plan(const void* const* sendbufs, void* const* recvbufs,
+                                      const size_t* counts, int ntensors, int nranks,
+                                      vc_dtype_t dtype, vc_order_t order, vc_bucket_tile_t* tiles,
+                                      int max_tiles, int* ntiles, size_t* bucket_count) {
+    if (ntiles == nullptr || bucket_count == nullptr) return VC_ERR_INVALID_ARGUMENT;
+    if (nranks < 1 || nranks > VC_MAX_RANKS || ntensors < 0 || max_tiles < 0)
+        return VC_ERR_INVALID_ARGUMENT;
+    const int es = esize(dtype);
+    if (es == 0) return VC_ERR_INVALID_ARGUMENT;
+    if (order < VC_ORDER_RING || order > VC_ORDER_DOUBLE_BINARY_TREE) return VC_ERR_INVALID_ARGUMENT;
+    const bool is_float = dtype == VC_FLOAT32 || dtype == VC_BFLOAT16;
+    if (order == VC_ORDER_RECURSIVE_HALVING && (nranks & (nranks - 1)) != 0)
+        return VC_ERR_UNSUPPORTED;
+    // floats: only the ring has a fused kernel; integers are order-free
+    if (is_float && order != VC_ORDER_RING) return VC_ERR_UNSUPPORTED;
+    if (ntensors > 0 && (sendbufs == nullptr || recvbufs == nullptr || counts == nullptr))
+        return VC_ERR_INVALID_ARGUMENT;
+
+    // the bucket layout: every tensor on a 16-byte boundary
+    const unsigned long long align = 16 / es;
+    const unsigned long long limit = (1ULL << 62) / (unsigned long long)es;
+    std::vector<unsigned long long> base(ntensors);
+    unsigned long long off = 0;
+    std::vector<Span> ins, outs;
+    for (int k = 0; k < ntensors; ++k) {
+        base[k] = off;
+        const unsigned long long c = counts[k];
+        if (c > limit || off + c > limit) return VC_ERR_INVALID_ARGUMENT;
+        off = (off + c + align - 1) / align * align;
+        if (c == 0) continue;
+        const size_t bytes = (size_t)c * es;
+        for (int r = 0; r < nranks; ++r) {
+            const void* in = sendbufs[(size_t)k * nranks + r];
+            const void* out = recvbufs[(size_t)k * nranks + r];
+            if (in == nullptr || out == nullptr) return VC_ERR_INVALID_ARGUMENT;
+            if (reinterpret_cast<uintptr_t>(in) % es || reinterpret_cast<uintptr_t>(out) % es)
+                return VC_ERR_INVALID_ARGUMENT;
+            const uintptr_t i0 = reinterpret_cast<uintptr_t>(in);
+            const uintptr_t o0 = reinterpret_cast<uintptr_t>(out);
+            ins.push_back({i0, i0 + bytes, k, r});
+            outs.push_back({o0, o0 + bytes, k, r});
+        }
+    }
+    const vc_status_t a = check_bucket_alias(ins, outs);
+    if (a != VC_SUCCESS) return a;
+
+    // tiles: at most VC_BUCKET_TILE_MAX_BYTES, never across a ring chunk; a
+    // tile that starts off the vector grid ends where the grid resumes, so
+    // the tiles after it are aligned again (when the tensor's bases are)
+    const unsigned long long total = off;
+    const unsigned long long q = total == 0 ? 1 : (total + nranks - 1) / nranks;
+    const unsigned long long tile_max = VC_BUCKET_TILE_MAX_BYTES / es;
+    std::vector<vc_bucket_tile_t> plan;
+    for (int k = 0; k < ntensors; ++k) {
+        const unsigned long long c = counts[k];
+        unsigned long long pos = 0;
+        while (pos < c) {
+            const unsigned long long b = base[k] + pos;
+            const unsigned long long chunk_end = (b / q + 1) * q;
+            unsigned long long len = std::min(c - pos, std::min(tile_max, chunk_end - b));
+            if (pos % align != 0) len = std::min(len, align - pos % align);
+            bool vec = true;
+            for (int r = 0; r < nranks && vec; ++r) {
+                const uintptr_t i = reinterpret_cast<uintptr_t>(sendbufs[(size_t)k * nranks + r]);
+                const uintptr_t o = reinterpret_cast<uintptr_t>(recvbufs[(size_t)k * nranks + r]);
+                vec = ((i + pos * es) % 16 == 0) && ((o + pos * es) % 16 == 0);
+            }
+            plan.push_back({(long long)b, (long long)pos, (long long)len, k, vec ? 1 : 0});
+            pos += len;
+        }
+    }
+    if (plan.size() > (size_t)0x7fffffff) return VC_ERR_INVALID_ARGUMENT;
+    *ntiles = (int)plan.size();
+    *bucket_count = (size_t)total;
+    if (tiles == nullptr) return VC_SUCCESS;
+    if (max_tiles < *ntiles) return VC_ERR_INVALID_ARGUMENT;
+    if (!plan.empty()) std::memcpy(tiles, plan.data(), plan.size() * sizeof(vc_bucket_tile_t));
+    return VC_SUCCESS;
+}
+
+extern "C" vc_status_t vc_all_reduce_bucket(const vc_bucket_tile_t* dev_tiles, int ntiles,
+                                            const void* const* dev_sendbufs,
+                                            void* const* dev_recvbufs, int nranks,
+                                            size_t bucket_count, vc_dtype_t dtype, vc_op_t op,
+                                            vc_stream_t stream) {
+    if (nranks < 1 || nranks > VC_MAX_RANKS || ntiles < 0) return VC_ERR_INVALID_ARGUMENT;
+    if (esize(dtype) == 0 || op < VC_SUM || op > VC_AVG) return VC_ERR_INVALID_ARGUMENT;
+    if (ntiles == 0) return VC_SUCCESS;
+    if (dev_tiles == nullptr || dev_sendbufs == nullptr || dev_recvbufs == nullptr ||
+        bucket_count == 0)
+        return VC_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(dev_tiles) % 8 != 0) return VC_ERR_INVALID_ARGUMENT;
+    if (launch_failure_injected()) return VC_ERR_CUDA;
+    BucketParams p;
+    p.tiles = dev_tiles;
+    p.in = dev_sendbufs;
+    p.out = dev_recvbufs;
+    p.q = (long long)((bucket_count + nranks - 1) / nranks);
+    p.ntiles = ntiles;
+    p.n = nranks;
+    p.avg = op == VC_AVG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (dtype) {
+    case VC_INT32: e = launch_bucket_i32(p, op, st); break;
+    case VC_INT64: e = launch_bucket_i64(p, op, st); break;
+    case VC_FLOAT32: e = launch_bucket_f32(p, op, st); break;
+    case VC_BFLOAT16: e = launch_bucket_bf16(p, op, st); break;
+    default: return VC_ERR_INVALID_ARGUMENT;
+    }
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+}

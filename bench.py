@@ -718,8 +718,10 @@ def transformer_grad_shapes(layers: int = 12, hidden: int = 1024, vocab: int = 3
 def bucket_report(torch, vc, args, dev):
     """One AllReduce per gradient tensor against one per 25 MiB bucket (the
     pages' DDP buckets), on 8 virtual ranks of bf16 gradients: with the
-    gradients as bucket views (no copy) and with packing; the per-tensor and
-    bucket loops also replayed from a CUDA graph (launch cost amortised)."""
+    gradients as bucket views (no copy), with packing (three launches per
+    bucket) and fused (one launch per bucket, the tensors reduced where they
+    are); the per-tensor and bucket loops also replayed from a CUDA graph
+    (launch cost amortised)."""
     from allreduce_reducescatter_allgather_gb300 import bucketing
     n = 8
     shapes = transformer_grad_shapes()
@@ -745,7 +747,10 @@ def bucket_report(torch, vc, args, dev):
         gb.all_reduce(op=args.op, order=args.order)
 
     def packed():
-        gb.all_reduce_tensors(op=args.op, order=args.order)
+        gb.all_reduce_tensors(op=args.op, order=args.order, fused=False)
+
+    def fused():
+        gb.all_reduce_tensors(op=args.op, order=args.order, fused=True)
 
     def t_ms(fn, reps=10):
         for _ in range(3):
@@ -778,7 +783,9 @@ def bucket_report(torch, vc, args, dev):
                                ("per_tensor_graph", graphed(per_tensor), len(shapes)),
                                ("bucket_views", views, len(gb.buckets)),
                                ("bucket_views_graph", graphed(views), len(gb.buckets)),
-                               ("bucket_packed", packed, 3 * len(gb.buckets))):
+                               ("bucket_packed", packed, 3 * len(gb.buckets))) + (
+            (("bucket_fused", fused, len(gb.buckets)),) if gb.fused_supported(args.order)
+            else ()):
         ms = t_ms(fn)
         out[name] = {"us": round(ms * 1e3, 1), "allreduce_gbs": round(ar_bytes / ms / 1e6, 1),
                      "launches": launches}

@@ -222,6 +222,80 @@ typedef struct {
  * launches nothing. */
 vc_status_t vc_copy_tiles(const vc_copy_tile_t *dev_tiles, int ntiles, vc_stream_t stream);
 
+/* ---- fused AllReduce of a gradient bucket --------------------------------
+ *
+ * The pages' DDP buckets ("通信与互联（01）" 三.1 and 九.1; "Ring AllReduce
+ * 核心流程" 4): many small gradient tensors are reduced as one bucket so that
+ * one large collective replaces many small ones.  When the tensors cannot
+ * live inside the bucket buffer, packing them in and out around the
+ * AllReduce moves every byte three times.  These two calls reduce the
+ * tensors where they are, in one launch, with the bits of the packed path.
+ *
+ * The bucket: the tensors in the order given, tensor k at element offset
+ * b_k of the bucket, where b_0 = 0 and b_{k+1} is b_k + counts[k] rounded up
+ * to a multiple of 16 bytes; bucket_count is the end of the last tensor
+ * rounded up the same way.  Element j of tensor k gets, on every rank, the
+ * value the ring-order AllReduce (VC_ORDER_RING) of the bucket gives at
+ * bucket index b_k + j, the gaps between tensors holding zeros; with the
+ * tensors packed into one buffer per rank, vc_all_reduce on that buffer
+ * gives the same bits. */
+
+/* One tile of a fused bucket AllReduce, as vc_bucket_plan writes it: count
+ * consecutive elements of tensor `tensor`, starting at its element
+ * tensor_offset, which stand at element bucket_offset of the bucket.  A
+ * tile never crosses a ring chunk boundary of the bucket (a multiple of
+ * vc_shard_count(bucket_count, nranks)).  flags bit 0: every rank's input
+ * and output address of the tile's first element is 16-byte aligned. */
+typedef struct {
+    long long bucket_offset;
+    long long tensor_offset;
+    long long count;
+    int tensor;
+    int flags;
+} vc_bucket_tile_t;
+
+/* The largest tile vc_bucket_plan makes, per rank.  (Measured on GB300 with
+ * a 351 MiB set of 145 bf16 tensors on 8 ranks: 64 KiB tiles ran 13 % behind
+ * the in-bucket AllReduce, 16 KiB tiles 4 %: more, smaller tiles balance the
+ * last wave of blocks.) */
+#define VC_BUCKET_TILE_MAX_BYTES (1u << 14)
+
+/* Plans a fused bucket AllReduce (host only; launches nothing).
+ * sendbufs, recvbufs: HOST arrays of ntensors * nranks DEVICE pointers,
+ *   entry [k * nranks + r] = tensor k of rank r (counts[k] elements);
+ *   recvbufs may equal sendbufs entry by entry (in place, as DDP does).
+ * counts: HOST array of ntensors element counts (0 allowed).
+ * dtype, order: floats take VC_ORDER_RING only (VC_ERR_UNSUPPORTED
+ *   otherwise); integers take every order (their result is the same in every
+ *   order), recursive halving with a power-of-two nranks.
+ * tiles: HOST array of max_tiles entries receiving the plan, or NULL to ask
+ *   for the number of tiles only.
+ * *ntiles receives the number of tiles the plan needs, *bucket_count the
+ *   bucket's element count.
+ * Errors (nothing written to tiles): VC_ERR_INVALID_ARGUMENT for a bad
+ * argument, a NULL or misaligned pointer of a non-empty tensor, or
+ * max_tiles < *ntiles (with *ntiles still set); VC_ERR_ALIAS when an output
+ * range overlaps another output range, or an input range other than its own
+ * input in place; VC_ERR_UNSUPPORTED as above. */
+vc_status_t vc_bucket_plan(const void *const *sendbufs, void *const *recvbufs,
+                           const size_t *counts, int ntensors, int nranks, vc_dtype_t dtype,
+                           vc_order_t order, vc_bucket_tile_t *tiles, int max_tiles,
+                           int *ntiles, size_t *bucket_count);
+
+/* Runs a plan from vc_bucket_plan in one launch on `stream`.
+ * dev_tiles: DEVICE array of the ntiles tiles (8-byte aligned).
+ * dev_sendbufs, dev_recvbufs: DEVICE arrays holding the same ntensors *
+ *   nranks pointer tables that were planned.
+ * bucket_count: the value the plan returned.
+ * op: any vc_op_t (AVG divides by nranks).
+ * The tables live in device memory, so the library checks only the scalar
+ * arguments here; tables that differ from the planned ones are undefined
+ * behaviour, as for any device copy.  ntiles == 0 launches nothing. */
+vc_status_t vc_all_reduce_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
+                                 const void *const *dev_sendbufs, void *const *dev_recvbufs,
+                                 int nranks, size_t bucket_count, vc_dtype_t dtype, vc_op_t op,
+                                 vc_stream_t stream);
+
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
  * 32 MiB on every GPU that loads this library, held until the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)

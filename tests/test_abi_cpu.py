@@ -55,7 +55,8 @@ def test_header_declares_the_entry_points():
     assert names == sorted(["vc_shard_count", "vc_reduce_scatter", "vc_all_gather",
                             "vc_all_reduce", "vc_all_reduce_decomposed", "vc_reduce",
                             "vc_broadcast", "vc_copy_tiles",
-                            "vc_all_reduce_decomposed_noalloc", "vc_status_string"])
+                            "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan",
+                            "vc_all_reduce_bucket", "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -347,3 +348,133 @@ def test_alias_check_agrees_with_pairwise_rule(vc):
             outs[r] = ins[rnd.randrange(n)] + 16 * rnd.randrange(0, nb // 16)
         want = ALIAS if trial % 2 else CUDA
         assert rs(vc, ins, outs, n, M) == want, trial
+
+
+# ------------------------------------------------------- fused bucket plan --
+
+def _plan(vc, ins, outs, counts, n, dtype=F32, order=RING, max_tiles=None):
+    """vc_bucket_plan on host pointer tables ins[k][r] / outs[k][r]; returns
+    (status, tiles, ntiles, bucket_count)."""
+    import ctypes
+    from allreduce_reducescatter_allgather_gb300._binding import BucketTile
+    L = vc.lib()
+    flat_in = [ins[k][r] for k in range(len(counts)) for r in range(n)]
+    flat_out = [outs[k][r] for k in range(len(counts)) for r in range(n)]
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    ti = (ctypes.c_void_p * max(1, len(flat_in)))(*flat_in)
+    to = (ctypes.c_void_p * max(1, len(flat_out)))(*flat_out)
+    cnt = (ctypes.c_size_t * max(1, len(counts)))(*counts)
+    nt, bc = ctypes.c_int(-1), ctypes.c_size_t(0)
+    args = (ctypes.cast(ti, vpp), ctypes.cast(to, vpp), cnt, len(counts), n, dtype, order)
+    st = L.vc_bucket_plan(*args, None, 0, ctypes.byref(nt), ctypes.byref(bc))
+    if st != SUCCESS:
+        return st, None, nt.value, bc.value
+    cap = nt.value if max_tiles is None else max_tiles
+    tiles = (BucketTile * max(1, cap))()
+    st = L.vc_bucket_plan(*args, tiles, cap, ctypes.byref(nt), ctypes.byref(bc))
+    return st, [tiles[i] for i in range(nt.value)] if st == SUCCESS else None, nt.value, bc.value
+
+
+def _layout(counts, es):
+    """Bucket offsets as the header defines them: each tensor at the end of
+    the previous one rounded up to 16 bytes."""
+    align, off, base = 16 // es, 0, []
+    for c in counts:
+        base.append(off)
+        off = -(-(off + c) // align) * align
+    return base, off
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bucket_plan_tiles_partition_the_tensors(vc, seed):
+    """Tiles cover every element of every tensor exactly once, in order;
+    each sits at the tensor's bucket offset plus its tensor offset; none
+    crosses a ring chunk (a multiple of ceil(bucket_count / N)); none is
+    larger than 16 KiB; flags bit 0 is set exactly when every rank's input
+    and output address of the tile start is 16-byte aligned."""
+    import random
+    rng = random.Random(seed)
+    es = [4, 8, 4, 2][seed % 4]
+    dt = {4: F32, 8: I64, 2: BF16}[es] if seed % 4 != 2 else I32
+    n = rng.choice([1, 2, 3, 4, 8, 12])
+    counts = [rng.choice([0, 1, 3, 7, 100, 4096, 20000, 70001]) for _ in range(rng.randint(1, 9))]
+    # one allocation per (tensor, rank): 1 MiB apart; some bases off 16 bytes
+    ins = [[(1 << 40) + ((k * n + r) << 22) + es * rng.choice([0, 0, 1]) for r in range(n)]
+           for k in range(len(counts))]
+    outs = [[(1 << 41) + ((k * n + r) << 22) + es * rng.choice([0, 0, 3]) for r in range(n)]
+            for k in range(len(counts))]
+    st, tiles, ntiles, bc = _plan(vc, ins, outs, counts, n, dtype=dt)
+    assert st == SUCCESS
+    base, total = _layout(counts, es)
+    assert bc == total
+    q = -(-total // n) if total else 1
+    seen = {k: 0 for k in range(len(counts))}
+    for t in tiles:
+        assert t.count > 0 and t.count * es <= 16 << 10   # VC_BUCKET_TILE_MAX_BYTES
+        assert t.tensor_offset == seen[t.tensor], "tiles of a tensor follow each other"
+        seen[t.tensor] += t.count
+        assert t.bucket_offset == base[t.tensor] + t.tensor_offset
+        assert t.bucket_offset // q == (t.bucket_offset + t.count - 1) // q, "crosses a chunk"
+        aligned = all((ins[t.tensor][r] + t.tensor_offset * es) % 16 == 0 and
+                      (outs[t.tensor][r] + t.tensor_offset * es) % 16 == 0 for r in range(n))
+        assert bool(t.flags & 1) == aligned
+    assert seen == {k: c for k, c in enumerate(counts)}
+    assert ntiles == len(tiles)
+
+
+def test_bucket_plan_realigns_after_a_chunk_split(vc):
+    """A tile that starts off the vector grid (after a chunk boundary) is cut
+    where the grid resumes, so an aligned tensor's later tiles stay aligned."""
+    n, counts = 3, [100, 50_004]   # fp32: total 50_104, q = 16_702 (not a multiple of 4)
+    ins = [[(1 << 40) + ((k * n + r) << 22) for r in range(n)] for k in range(2)]
+    st, tiles, _, bc = _plan(vc, ins, ins, counts, n)
+    assert st == SUCCESS and bc == 50_104
+    unaligned = [t for t in tiles if not t.flags & 1]
+    # chunk 1 starts at bucket 16_702 = tensor offset 16_602 (2 past the grid):
+    # one 2-element tile, then aligned again; chunk 2 starts on the grid
+    assert [(t.tensor_offset, t.count) for t in unaligned] == [(16_602, 2)]
+
+
+def test_bucket_plan_rules(vc):
+    n = 4
+    ins = [fake(n, (1 << 40) + k * (1 << 30)) for k in range(2)]
+    outs = [fake(n, (1 << 42) + k * (1 << 30)) for k in range(2)]
+    counts = [1000, 333]
+    assert _plan(vc, ins, outs, counts, n)[0] == SUCCESS
+    assert _plan(vc, ins, ins, counts, n)[0] == SUCCESS                 # in place
+    # floats: ring only; integers: every order (RH needs a power of two)
+    assert _plan(vc, ins, outs, counts, n, order=TREE)[0] == UNSUPPORTED
+    assert _plan(vc, ins, outs, counts, n, dtype=I64, order=DTREE)[0] == SUCCESS
+    assert _plan(vc, [i[:3] for i in ins], [o[:3] for o in outs], counts, 3, dtype=I32,
+                 order=RH)[0] == UNSUPPORTED
+    # aliasing: two outputs overlap; an input overlaps another tensor's
+    # output; an input overlaps its own output but not exactly
+    bad = [list(o) for o in outs]
+    bad[1][2] = outs[0][2] + 400
+    assert _plan(vc, ins, bad, counts, n)[0] == ALIAS
+    bad = [list(o) for o in outs]
+    bad[1][0] = ins[0][0] + 64
+    assert _plan(vc, ins, bad, counts, n)[0] == ALIAS
+    bad = [list(i) for i in ins]
+    bad[0][1] = ins[0][1] + 16
+    assert _plan(vc, ins, bad, counts, n)[0] == ALIAS
+    # null or misaligned pointers of non-empty tensors; empty ones are ignored
+    bad = [list(i) for i in ins]
+    bad[1][3] = 0
+    assert _plan(vc, bad, outs, counts, n)[0] == INVALID
+    assert _plan(vc, bad, outs, [1000, 0], n)[0] == SUCCESS
+    bad[1][3] = ins[1][3] + 2
+    assert _plan(vc, bad, outs, counts, n)[0] == INVALID
+    # too few tiles: error, with the needed count reported
+    st, _, ntiles, _ = _plan(vc, ins, outs, counts, n, max_tiles=1)
+    assert st == INVALID and ntiles >= 2
+
+
+def test_all_reduce_bucket_checks(vc):
+    L = vc.lib()
+    assert L.vc_all_reduce_bucket(None, 0, None, None, 4, 100, F32, SUM, None) == SUCCESS
+    assert L.vc_all_reduce_bucket(1 << 40, 5, 1 << 41, 1 << 42, 4, 100, F32, 9, None) == INVALID
+    assert L.vc_all_reduce_bucket(1 << 40, 5, 1 << 41, 1 << 42, 0, 100, F32, SUM, None) == INVALID
+    assert L.vc_all_reduce_bucket((1 << 40) + 4, 5, 1 << 41, 1 << 42, 4, 100, F32, SUM,
+                                  None) == INVALID
+    assert L.vc_all_reduce_bucket(1 << 40, 5, 1 << 41, 1 << 42, 4, 100, F32, SUM, None) == CUDA

@@ -107,19 +107,21 @@ def test_bucket_views_and_packing_match_oracle(genv, dtype, op, order):
     for r in range(n):
         for t, v in enumerate(gb.views(r)):
             assert_bits_equal(to_host(v.reshape(-1), dtype), want[r][t], dtype, f"view r{r} t{t}")
-    # packing: separately allocated tensors, packed, reduced, unpacked
-    for b in gb.buckets:
-        for buf in b.buffers:
-            buf.zero_()
-    grads = [[to_dev(grads_np[r][t]).view(SHAPES[t]).clone() for t in range(len(SHAPES))]
-             for r in range(n)]
-    gb.bind(grads)
-    gb.all_reduce_tensors(op=op, order=order)
-    torch.cuda.synchronize()
-    for r in range(n):
-        for t in range(len(SHAPES)):
-            assert_bits_equal(to_host(grads[r][t].reshape(-1), dtype), want[r][t], dtype,
-                              f"packed r{r} t{t}")
+    # separately allocated tensors: packed, reduced, unpacked; and fused
+    # (one launch per bucket) where the order allows it
+    for fused in (False, True):
+        for b in gb.buckets:
+            for buf in b.buffers:
+                buf.zero_()
+        grads = [[to_dev(grads_np[r][t]).view(SHAPES[t]).clone() for t in range(len(SHAPES))]
+                 for r in range(n)]
+        gb.bind(grads)
+        gb.all_reduce_tensors(op=op, order=order, fused=fused)
+        torch.cuda.synchronize()
+        for r in range(n):
+            for t in range(len(SHAPES)):
+                assert_bits_equal(to_host(grads[r][t].reshape(-1), dtype), want[r][t], dtype,
+                                  f"fused={fused} r{r} t{t}")
 
 
 @pytest.mark.gpu
@@ -143,3 +145,80 @@ def test_bucketed_equals_per_tensor_for_chunk_free_orders(genv):
             vc.vc_all_reduce([src[r][t] for r in range(n)], ref, order=order)
             for r in range(n):
                 assert torch.equal(grads[r][t], ref[r])
+
+
+FUSED_SHAPES = [(5,), (16_381,), (0,), (3, 7), (70_001,), (1,), (4096,), (33_333,)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "avg"),
+                                      ("int32", "prod"), ("int64", "min")])
+@pytest.mark.parametrize("n", [3, 8, 12])
+def test_fused_bucket_matches_oracle(genv, dtype, op, n):
+    """vc_all_reduce_bucket against the oracle's ring AllReduce of the packed
+    bucket (each tensor at the previous one's end rounded up to 16 bytes,
+    zeros between), out of place, with every other tensor a view whose base
+    is one element off the 16-byte grid (the element-by-element path)."""
+    torch, vc, bk, dev = genv
+    tdt = {"float32": torch.float32, "bfloat16": torch.bfloat16, "int32": torch.int32,
+           "int64": torch.int64}[dtype]
+    es = torch.empty(0, dtype=tdt).element_size()
+    dist = "uniform_pm1" if dtype in ("float32", "bfloat16") else "uniform_int"
+    kw = {} if dist == "uniform_pm1" else {"lo": -3, "hi": 3}
+    counts = [int(np.prod(s)) for s in FUSED_SHAPES]
+    host = [[si.generate_rank(dtype, dist, 50 + k, r, counts[k], **kw) for k in range(len(counts))]
+            for r in range(n)]
+
+    def to_dev(a, shift):
+        t = torch.from_numpy(a.view(np.int16) if dtype == "bfloat16" else a)
+        t = t.view(tdt) if dtype == "bfloat16" else t
+        big = torch.empty(a.size + shift, dtype=tdt, device=dev)
+        big[shift:].copy_(t.to(dev))
+        return big[shift:]
+
+    ins = [[to_dev(host[r][k], k % 2) for k in range(len(counts))] for r in range(n)]
+    outs = [[to_dev(np.zeros_like(host[r][k]), (k + 1) % 2) for k in range(len(counts))]
+            for r in range(n)]
+    plan = vc.BucketAllReduce(ins, outs)
+    plan(op=op)
+    torch.cuda.synchronize()
+    # the oracle: the packed bucket, its ring AllReduce, sliced back
+    align, off, base = 16 // es, 0, []
+    for c in counts:
+        base.append(off)
+        off = -(-(off + c) // align) * align
+    assert plan.bucket_count == off
+    st = oracle.NP_STORAGE[dtype]
+    bufs = [np.zeros(off, st) for _ in range(n)]
+    for r in range(n):
+        for k, c in enumerate(counts):
+            bufs[r][base[k]:base[k] + c] = host[r][k]
+    ys = oracle.all_reduce(bufs, dtype, op, "ring")
+    for r in range(n):
+        for k, c in enumerate(counts):
+            assert_bits_equal(to_host(outs[r][k], dtype), ys[r][base[k]:base[k] + c], dtype,
+                              f"N={n} rank {r} tensor {k}")
+            # inputs untouched (out of place)
+            assert_bits_equal(to_host(ins[r][k], dtype), host[r][k], dtype, "input kept")
+
+
+@pytest.mark.gpu
+def test_fused_bucket_in_place_equals_bucket_views(genv):
+    """In place on the transformer-shaped gradient set: the fused call gives
+    the bits of the bucket views path, bucket by bucket."""
+    torch, vc, bk, dev = genv
+    n = 8
+    shapes = [(1024, 1024), (1024,), (4096, 1024), (1024, 4096), (32000, 1024), (1000, 3)]
+    gb = bk.GradientBuckets(shapes, torch.bfloat16, n, dev)
+    src = [[torch.randn(s, device=dev).to(torch.bfloat16) for s in shapes] for _ in range(n)]
+    for r in range(n):
+        for t, v in enumerate(gb.views(r)):
+            v.copy_(src[r][t])
+    grads = [[g.clone() for g in row] for row in src]
+    gb.bind(grads)
+    gb.all_reduce(op="sum", order="ring")
+    gb.all_reduce_tensors(op="sum", order="ring", fused=True)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for t, v in enumerate(gb.views(r)):
+            assert torch.equal(grads[r][t], v)
