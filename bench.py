@@ -74,12 +74,21 @@ def _code_only(text: str) -> str:
     return "\n".join(ln for ln in lines if ln.strip())
 
 
+# The sources that build and launch the measured kernels (vc_ar_kernel,
+# vc_rs_kernel, vc_ag_kernel): the kernels and folds, the instance dispatch,
+# and the host side that sizes the grids.
+KERNEL_SOURCES = ("vc_device.cuh", "vc_launch.cuh", "vc_reduce_inst.cu",
+                  "vc_reduce_dispatch.cu", "vc_api.cu")
+
+
 def source_digest() -> str:
-    """Digest of the CUDA sources' code (comments and blank lines removed)."""
+    """Digest of the code (comments and blank lines removed) of the sources
+    that build and launch the measured kernels."""
     h = hashlib.sha256()
-    for f in sorted((ROOT / "allreduce_reducescatter_allgather_gb300" / "csrc").glob("*")):
-        h.update(f.name.encode())
-        h.update(_code_only(f.read_text()).encode())
+    csrc = ROOT / "allreduce_reducescatter_allgather_gb300" / "csrc"
+    for name in KERNEL_SOURCES:
+        h.update(name.encode())
+        h.update(_code_only((csrc / name).read_text()).encode())
     return h.hexdigest()[:16]
 
 
