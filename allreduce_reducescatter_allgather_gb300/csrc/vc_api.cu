@@ -200,10 +200,11 @@ vc_status_t launch_broadcast(const void* src, void* const* out, int nout, size_t
 
 // SMs of the current device, queried once per device; -1 on error.
 int sm_count() {
+    constexpr int kMaxDevices = 64;
     static std::mutex mu;
-    static int count[VC_MAX_RANKS] = {0};
+    static int count[kMaxDevices] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= VC_MAX_RANKS) return -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     std::lock_guard<std::mutex> lock(mu);
     if (count[dev] == 0) {
         int v = 0;
