@@ -243,6 +243,24 @@ def time_oracle(workload: dict, op: str, order: str, seconds: float, window: int
     return b * steps / el / 1e9, steps, el
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or ""."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
+
+
 def _oracle_worker(job):
     """One process of the all-cores oracle timing: its own window."""
     workload, op, order, seconds, window, start = job
@@ -473,6 +491,7 @@ def run_ours(args, workload: dict):
                                      window=1 << 22)
         line["cpu_baseline"] = {
             "value": round(g, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{steps} oracle steps (fused AR + decomposed AR) over the first "
                       f"{min(1 << 22, M)} elements of each of the {n} ranks, "
                       f"{secs:.1f} s on one host core"}
