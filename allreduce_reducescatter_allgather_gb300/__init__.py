@@ -7,7 +7,7 @@ order (ring, recursive halving or tree).  This package is the thin ctypes
 binding with the same names as the C entry points.
 """
 from ._binding import (  # noqa: F401
-    BucketAllReduce,
+    BucketPlan,
     DTYPES,
     MAX_RANKS,
     OPS,

@@ -30,7 +30,7 @@ MAX_RANKS = 64
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
            "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles",
            "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan", "vc_all_reduce_bucket",
-           "vc_status_string")
+           "vc_reduce_scatter_bucket", "vc_status_string")
 
 
 class BucketTile(ctypes.Structure):
@@ -74,8 +74,10 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(BucketTile), i32, ctypes.POINTER(i32),
                                      ctypes.POINTER(sz)]
         L.vc_all_reduce_bucket.argtypes = [vp, i32, vp, vp, i32, sz, i32, i32, vp]
+        L.vc_reduce_scatter_bucket.argtypes = [vp, i32, vp, vpp, i32, sz, i32, i32, vp]
         L.vc_bucket_plan.restype = i32
         L.vc_all_reduce_bucket.restype = i32
+        L.vc_reduce_scatter_bucket.restype = i32
         for f in ("vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
                   "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles"):
             getattr(L, f).restype = i32
@@ -382,14 +384,16 @@ def vc_all_reduce_decomposed_noalloc(sendbufs, recvbufs=None, op: str = "sum",
 
 # ------------------------------------------------------------ fused buckets --
 
-class BucketAllReduce:
-    """The AllReduce of a gradient bucket whose tensors stay where they are
-    (vc_bucket_plan + vc_all_reduce_bucket): tensors[r][k] is tensor k of
-    rank r, out[r][k] its output (None: in place).  The bucket holds the
-    tensors in the order given, each on a 16-byte boundary; every element
-    gets the bits the ring-order AllReduce of that bucket gives it.  Planned
-    once (pointer checks, aliasing, tiles); each call is one launch.  The
-    plan keeps the tensors' addresses: make a new one if they change."""
+class BucketPlan:
+    """A gradient bucket whose tensors stay where they are (vc_bucket_plan):
+    tensors[r][k] is tensor k of rank r, out[r][k] its AllReduce output
+    (None: in place).  The bucket holds the tensors in the order given, each
+    on a 16-byte boundary.  all_reduce() (also the call operator) gives every
+    element the bits the ring-order AllReduce of that bucket gives it;
+    reduce_scatter() writes shard r of the bucket's ring-order ReduceScatter
+    to rank r's shard.  Planned once (pointer checks, aliasing, tiles); each
+    call is one launch.  The plan keeps the tensors' addresses: make a new
+    one if they change."""
 
     def __init__(self, tensors, out=None, order: str = "ring"):
         import torch
@@ -435,11 +439,45 @@ class BucketAllReduce:
         self.in_ptrs = torch.tensor(ins, dtype=torch.int64).to(dev)
         self.out_ptrs = torch.tensor(outs, dtype=torch.int64).to(dev)
         self._keep = (tensors, out)
+        self._checked_shards = None
         self.host_tiles = tiles
 
+    @property
+    def shard_count(self) -> int:
+        """q: the elements of one rank's shard of the bucket."""
+        return vc_shard_count(self.bucket_count, self.nranks)
+
     def __call__(self, op: str = "sum", stream=None):
+        self.all_reduce(op=op, stream=stream)
+
+    def reduce_scatter(self, shards, op: str = "sum", stream=None):
+        """shards[r]: rank r's output, shard_count elements of the bucket's
+        dtype on its device; disjoint from each other and from the tensors."""
+        if len(shards) != self.nranks:
+            raise ValueError("one shard per rank")
+        key = tuple(t.data_ptr() for t in shards)
+        if key != self._checked_shards:  # checked once per set of shard buffers
+            _check_tensors("shards", shards, self.dtype, self.shard_count, self.device)
+            for t in shards:
+                for row in self._keep[0]:
+                    for g in row:
+                        if g.numel() and _overlaps(t, g):
+                            raise ValueError("a shard overlaps a bucket tensor")
+            self._checked_shards = key
+        check_status(lib().vc_reduce_scatter_bucket(
+            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
+            ctypes.c_void_p(self.in_ptrs.data_ptr()), _ptrs(shards), self.nranks,
+            self.bucket_count, DTYPES[self.dtype], OPS[op], _stream(stream, self.device)))
+
+    def all_reduce(self, op: str = "sum", stream=None):
         check_status(lib().vc_all_reduce_bucket(
             ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
             ctypes.c_void_p(self.in_ptrs.data_ptr()), ctypes.c_void_p(self.out_ptrs.data_ptr()),
             self.nranks, self.bucket_count, DTYPES[self.dtype], OPS[op],
             _stream(stream, self.device)))
+
+
+def _overlaps(a, b) -> bool:
+    """Whether two tensors' byte ranges overlap."""
+    a0, b0 = a.data_ptr(), b.data_ptr()
+    return a0 < b0 + b.numel() * b.element_size() and b0 < a0 + a.numel() * a.element_size()

@@ -69,7 +69,8 @@ class _Bucket:
     pack_tiles: object = None    # device table for vc_copy_tiles (tensors -> bucket)
     unpack_tiles: object = None  # (bucket -> tensors)
     ntiles: int = 0
-    fused: object = None         # BucketAllReduce over the bound tensors, in place
+    fused: object = None         # BucketPlan over the bound tensors, in place
+    shards: object = None        # ReduceScatter outputs, one per rank
 
 
 class GradientBuckets:
@@ -131,6 +132,30 @@ class GradientBuckets:
         for c in self._calls(op, order):
             c(stream=stream)
 
+    # --------------------------------------------------- ReduceScatter --
+    def shards(self, bucket: int):
+        """Rank r's shard of bucket `bucket` (ceil(count / N) elements each),
+        the output of the ReduceScatter calls; allocated on first use."""
+        b = self.buckets[bucket]
+        if getattr(b, "shards", None) is None:
+            q = _binding.vc_shard_count(b.count, self.nranks)
+            b.shards = [self.torch.empty(q, dtype=self.dtype, device=self.device)
+                        for _ in range(self.nranks)]
+        return b.shards
+
+    def reduce_scatter(self, op: str = "sum", order: str = "ring", stream=None):
+        """ZeRO-style: one ReduceScatter per bucket, from the bucket buffers
+        into shards(bucket); returns the shards of every bucket."""
+        key = ("rs", op, order)
+        calls = self._prepared.get(key)
+        if calls is None:
+            calls = [_binding.prepare_reduce_scatter(b.buffers, self.shards(i), op=op, order=order)
+                     for i, b in enumerate(self.buckets)]
+            self._prepared[key] = calls
+        for c in calls:
+            c(stream=stream)
+        return [self.shards(i) for i in range(len(self.buckets))]
+
     # -------------------------------------------------------- packing --
     def _tiles(self, b: _Bucket, grads, to_bucket: bool):
         rows = []
@@ -163,7 +188,7 @@ class GradientBuckets:
             b.ntiles = len(pack)
             # the fused call lays the bucket out the same way: its tensors in
             # fill order, each on a 16-byte boundary
-            b.fused = _binding.BucketAllReduce(
+            b.fused = _binding.BucketPlan(
                 [[grads[r][t] for t in b.tensors] for r in range(self.nranks)])
             assert b.fused.bucket_count == b.count or not any(self.numels[t] for t in b.tensors)
         self.bound = grads
@@ -198,3 +223,27 @@ class GradientBuckets:
             c(stream=stream)
             _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.unpack_tiles.data_ptr()),
                                                   b.ntiles, s))
+
+    def reduce_scatter_tensors(self, op: str = "sum", order: str = "ring", stream=None,
+                               fused: bool = True):
+        """For the bound tensors: the bucket's ReduceScatter into
+        shards(bucket), with the bits of packing them first.  fused (when the
+        order allows it, see fused_supported): one launch per bucket, the
+        tensors read where they are; otherwise pack (one launch) and
+        ReduceScatter the bucket buffer (one launch).  Returns the shards."""
+        torch = self.torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        if fused and self.fused_supported(order):
+            if order == "recursive_halving" and self.nranks & (self.nranks - 1):
+                raise ValueError("recursive halving needs a power-of-two rank count")
+            for i, b in enumerate(self.buckets):
+                b.fused.reduce_scatter(self.shards(i), op=op, stream=stream)
+            return [self.shards(i) for i in range(len(self.buckets))]
+        import ctypes
+        L = _binding.lib()
+        s = ctypes.c_void_p(stream.cuda_stream)
+        for b in self.buckets:
+            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
+                                                  b.ntiles, s))
+        return self.reduce_scatter(op=op, order=order, stream=stream)

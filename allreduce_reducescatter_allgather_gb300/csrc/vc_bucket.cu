@@ -1,5 +1,6 @@
-// vc_bucket_plan / vc_all_reduce_bucket: the AllReduce of a gradient bucket
-// whose tensors stay where they are.
+// vc_bucket_plan / vc_all_reduce_bucket / vc_reduce_scatter_bucket: the
+// AllReduce or ReduceScatter of a gradient bucket whose tensors stay where
+// they are.
 //
 // A DDP bucket ("通信与互联（01）" 三.1 and 九.1) is a flat buffer per rank
 // into which many gradient tensors are packed, so one AllReduce replaces
@@ -67,6 +68,19 @@ vc_status_t check_bucket_alias(const std::vector<Span>& ins, std::vector<Span> o
         }
     }
     return VC_SUCCESS;
+}
+
+vc_status_t launch_bucket(const BucketParams& p, vc_dtype_t dtype, vc_op_t op, bool rs,
+                          cudaStream_t st) {
+    cudaError_t e;
+    switch (dtype) {
+    case VC_INT32: e = launch_bucket_i32(p, op, rs, st); break;
+    case VC_INT64: e = launch_bucket_i64(p, op, rs, st); break;
+    case VC_FLOAT32: e = launch_bucket_f32(p, op, rs, st); break;
+    case VC_BFLOAT16: e = launch_bucket_bf16(p, op, rs, st); break;
+    default: return VC_ERR_INVALID_ARGUMENT;
+    }
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
 }
 
 }  // namespace
@@ -167,22 +181,51 @@ extern "C" vc_status_t vc_all_reduce_bucket(const vc_bucket_tile_t* dev_tiles, i
         return VC_ERR_INVALID_ARGUMENT;
     if (reinterpret_cast<uintptr_t>(dev_tiles) % 8 != 0) return VC_ERR_INVALID_ARGUMENT;
     if (launch_failure_injected()) return VC_ERR_CUDA;
-    BucketParams p;
+    BucketParams p = {};
     p.tiles = dev_tiles;
     p.in = dev_sendbufs;
     p.out = dev_recvbufs;
     p.q = (long long)((bucket_count + nranks - 1) / nranks);
+    p.bucket_count = (long long)bucket_count;
     p.ntiles = ntiles;
     p.n = nranks;
     p.avg = op == VC_AVG;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (dtype) {
-    case VC_INT32: e = launch_bucket_i32(p, op, st); break;
-    case VC_INT64: e = launch_bucket_i64(p, op, st); break;
-    case VC_FLOAT32: e = launch_bucket_f32(p, op, st); break;
-    case VC_BFLOAT16: e = launch_bucket_bf16(p, op, st); break;
-    default: return VC_ERR_INVALID_ARGUMENT;
+    return launch_bucket(p, dtype, op, false, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" vc_status_t vc_reduce_scatter_bucket(const vc_bucket_tile_t* dev_tiles, int ntiles,
+                                                const void* const* dev_sendbufs,
+                                                void* const* recvbufs, int nranks,
+                                                size_t bucket_count, vc_dtype_t dtype,
+                                                vc_op_t op, vc_stream_t stream) {
+    if (nranks < 1 || nranks > VC_MAX_RANKS || ntiles < 0) return VC_ERR_INVALID_ARGUMENT;
+    const int es = esize(dtype);
+    if (es == 0 || op < VC_SUM || op > VC_AVG) return VC_ERR_INVALID_ARGUMENT;
+    if (ntiles == 0) return VC_SUCCESS;
+    if (dev_tiles == nullptr || dev_sendbufs == nullptr || recvbufs == nullptr ||
+        bucket_count == 0)
+        return VC_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(dev_tiles) % 8 != 0) return VC_ERR_INVALID_ARGUMENT;
+    const unsigned long long q = (bucket_count + nranks - 1) / nranks;
+    if (q > (1ULL << 62) / (unsigned long long)es) return VC_ERR_INVALID_ARGUMENT;
+    std::vector<Span> shards;
+    for (int r = 0; r < nranks; ++r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(recvbufs[r]);
+        if (a == 0 || a % es != 0) return VC_ERR_INVALID_ARGUMENT;
+        shards.push_back({a, a + (uintptr_t)(q * es), -1, r});
     }
-    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+    const vc_status_t s = check_bucket_alias({}, shards);
+    if (s != VC_SUCCESS) return s;
+    if (launch_failure_injected()) return VC_ERR_CUDA;
+    BucketParams p = {};
+    p.tiles = dev_tiles;
+    p.in = dev_sendbufs;
+    p.out = nullptr;
+    for (int r = 0; r < nranks; ++r) p.shard[r] = recvbufs[r];
+    p.q = (long long)q;
+    p.bucket_count = (long long)bucket_count;
+    p.ntiles = ntiles;
+    p.n = nranks;
+    p.avg = op == VC_AVG;
+    return launch_bucket(p, dtype, op, true, static_cast<cudaStream_t>(stream));
 }

@@ -1,4 +1,4 @@
-// One element type's slice of the fused bucket AllReduce kernels.  The
+// One element type's slice of the fused bucket kernels.  The
 // build compiles this file once per type, with
 //   -DVC_T=<element type> -DVC_FN=<launcher name>.
 #include "vc_bucket_kernel.cuh"
@@ -8,7 +8,7 @@
 #endif
 
 namespace vc {
-cudaError_t VC_FN(const BucketParams& p, vc_op_t op, cudaStream_t st) {
-    return launch_bucket_op<VC_T>(p, op, st);
+cudaError_t VC_FN(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st) {
+    return launch_bucket_op<VC_T>(p, op, rs, st);
 }
 }  // namespace vc

@@ -1,7 +1,9 @@
-// The fused bucket AllReduce kernel (see vc_bucket.cu for the host side):
-// tiles of gradient tensors reduced where they are, in ring order with the
-// ring chunk of their place in the bucket.  Included by vc_bucket_inst.cu,
-// which the build compiles once per element type.
+// The fused bucket kernels (see vc_bucket.cu for the host side): tiles of
+// gradient tensors reduced where they are, in ring order with the ring chunk
+// of their place in the bucket, and written either back to the N ranks'
+// output tensors (AllReduce) or to the shard that owns the chunk
+// (ReduceScatter).  Included by vc_bucket_inst.cu, which the build compiles
+// once per element type.
 #pragma once
 
 #include <algorithm>
@@ -13,9 +15,11 @@ namespace vc {
 
 struct BucketParams {
     const vc_bucket_tile_t* tiles;
-    const void* const* in;  // [tensor * n + rank]
-    void* const* out;
-    long long q;  // ring chunk of the bucket: ceil(bucket_count / n)
+    const void* const* in;   // [tensor * n + rank]
+    void* const* out;        // AllReduce outputs, [tensor * n + rank]
+    void* shard[kMaxRanks];  // ReduceScatter outputs: shard r, q elements
+    long long q;             // ring chunk of the bucket: ceil(bucket_count / n)
+    long long bucket_count;
     int ntiles;
     int n;
     int avg;
@@ -38,42 +42,102 @@ template <class T> struct SharedScalarLoader {
     }
 };
 
-// One vector of consecutive tensor elements at tensor offset i0, reduced
-// over the N ranks in ring order for chunk c and written to the N outputs.
-template <class T, class Op>
-__device__ __forceinline__ void bucket_vector(const BucketParams& p, const void* const* s_in,
-                                              void* const* s_out, int c, long long i0) {
+// The reduced vector of tensor elements i0 .. i0+V-1 (bucket offset b0, in
+// chunk c) to its destination: every rank's output tensor (AllReduce), or
+// shard c at b0 - c*q (ReduceScatter; the shard's offset need not be on the
+// 16-byte grid).
+template <class T, bool RS, class Acc>
+__device__ __forceinline__ void bucket_store(const BucketParams& p, void* const* s_out, int c,
+                                             long long i0, long long b0, Acc& acc) {
     constexpr int V = Traits<T>::V;
-    SharedTableLoader<T> ld{s_in, i0};
-    auto acc = fold_ring_doubled<Op>(ld, p.n, c);
     if (p.avg) {
 #pragma unroll
         for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
     }
     const uint4 u = pack(acc, (T*)nullptr);
-    for (int r = 0; r < p.n; ++r) st16(static_cast<T*>(s_out[r]) + i0, u);
+    if constexpr (RS) {
+        st_aligned<sizeof(T)>(static_cast<T*>(p.shard[c]) + (b0 - (long long)c * p.q), u);
+    } else {
+        for (int r = 0; r < p.n; ++r) st16(static_cast<T*>(s_out[r]) + i0, u);
+    }
+}
+
+template <class T, class Op, bool RS>
+__device__ __forceinline__ void bucket_vector(const BucketParams& p, const void* const* s_in,
+                                              void* const* s_out, int c, long long i0,
+                                              long long b0) {
+    SharedTableLoader<T> ld{s_in, i0};
+    auto acc = fold_ring_doubled<Op>(ld, p.n, c);
+    bucket_store<T, RS>(p, s_out, c, i0, b0, acc);
+}
+
+template <class T, class Op, bool RS>
+__device__ __forceinline__ void bucket_element(const BucketParams& p, const void* const* s_in,
+                                               void* const* s_out, int c, long long i,
+                                               long long b) {
+    using A = typename Traits<T>::Acc;
+    SharedScalarLoader<T> ld{s_in, i};
+    A val = fold_ring_doubled<Op>(ld, p.n, c).x[0];
+    if (p.avg) val = avg_div(val, p.n);
+    if constexpr (RS) {
+        store1(static_cast<T*>(p.shard[c]) + (b - (long long)c * p.q), val);
+    } else {
+        for (int r = 0; r < p.n; ++r) store1(static_cast<T*>(s_out[r]) + i, val);
+    }
+}
+
+// ReduceScatter: the shard positions no tensor covers, from bucket offset
+// lo to hi.  Below bucket_count they are the gaps between tensors, which
+// the packed bucket holds as zeros on every rank: every op reduces zeros
+// to zero.  From bucket_count on they are the padding up to N*q: the op's
+// identity (0 for AVG), as the ReduceScatter pads.
+template <class T, class Op>
+__device__ __forceinline__ void bucket_fill(const BucketParams& p, long long lo, long long hi) {
+    using A = typename Traits<T>::Acc;
+    for (long long b = lo + threadIdx.x; b < hi; b += blockDim.x) {
+        const int c = (int)(b / p.q);
+        const A v = b < p.bucket_count ? A(0) : (p.avg ? A(0) : Identity<T, Op>::get());
+        store1(static_cast<T*>(p.shard[c]) + (b - (long long)c * p.q), v);
+    }
 }
 
 // NT > 0: N known at compile time; a thread loads the N x U operand vectors
 // of its U vectors (blockDim.x apart) into registers before folding any, as
 // the AllReduce kernel does.  NT == 0: a run-time N, one vector at a time.
-template <class T, class Op, int NT, int U>
-__global__ void __launch_bounds__(kThreads, NT > 0 ? 1 : 2)
-    vc_bucket_ar_kernel(const __grid_constant__ BucketParams p) {
-    using A = typename Traits<T>::Acc;
+// The tiles come in bucket order (vc_bucket_plan writes them so); for the
+// ReduceScatter, the block of tile t also fills the uncovered positions up
+// to the next tile (tile 0's block, those before it too).
+template <class T, class Op, int NT, int U, bool RS>
+__global__ void __launch_bounds__(kThreads, 2)
+    vc_bucket_kernel(const __grid_constant__ BucketParams p) {
     constexpr int V = Traits<T>::V;
     __shared__ const void* s_in[2 * kMaxRanks];
-    __shared__ void* s_out[kMaxRanks];
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const vc_bucket_tile_t tile = p.tiles[t];
+    __shared__ void* s_out[RS ? 1 : kMaxRanks];
+    // Software-pipelined tile set-up: while a block works on tile t it has
+    // already fetched tile t + gridDim.x's descriptor and (threads r < N)
+    // that tile's pointers, so a new tile starts after one shared-memory
+    // round trip instead of a chain of dependent global loads.
+    int t = blockIdx.x;
+    if (t >= p.ntiles) return;
+    vc_bucket_tile_t tile = p.tiles[t];
+    const int me = threadIdx.x;  // < kThreads; threads below n carry pointers
+    const void* my_in = me < p.n ? p.in[(long long)tile.tensor * p.n + me] : nullptr;
+    void* my_out = nullptr;
+    if constexpr (!RS) my_out = me < p.n ? p.out[(long long)tile.tensor * p.n + me] : nullptr;
+    for (; t < p.ntiles; t += gridDim.x) {
         __syncthreads();  // the last tile's readers are done with the tables
-        for (int r = threadIdx.x; r < p.n; r += blockDim.x) {
-            const void* a = p.in[(long long)tile.tensor * p.n + r];
-            s_in[r] = a;
-            s_in[r + p.n] = a;
-            s_out[r] = p.out[(long long)tile.tensor * p.n + r];
+        if (me < p.n) {
+            s_in[me] = my_in;
+            s_in[me + p.n] = my_in;
+            if constexpr (!RS) s_out[me] = my_out;
         }
         __syncthreads();
+        const int tn = t + gridDim.x;
+        vc_bucket_tile_t next_tile = tile;
+        if (tn < p.ntiles) next_tile = p.tiles[tn];
+        long long next_start = 0;  // ReduceScatter: where the next tile starts
+        if constexpr (RS)
+            next_start = t + 1 < p.ntiles ? p.tiles[t + 1].bucket_offset : (long long)p.n * p.q;
         const int c = (int)(tile.bucket_offset / p.q);  // the tile's ring chunk
         const long long nvec = (tile.flags & 1) ? tile.count / V : 0;
         const long long span = (long long)blockDim.x * U;
@@ -92,14 +156,9 @@ __global__ void __launch_bounds__(kThreads, NT > 0 ? 1 : 2)
                     for (int u = 0; u < U; ++u) {
                         PreLoader<T, NT, U> ld{buf, u};
                         auto acc = fold<Op, kOrderRing, NT>(ld, NT, c);
-                        if (p.avg) {
-#pragma unroll
-                            for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
-                        }
-                        const uint4 w = pack(acc, (T*)nullptr);
-                        const long long i0 = tile.tensor_offset + (v0 + (long long)u * blockDim.x) * V;
-#pragma unroll
-                        for (int r = 0; r < NT; ++r) st16(static_cast<T*>(s_out[r]) + i0, w);
+                        const long long j = (v0 + (long long)u * blockDim.x) * V;
+                        bucket_store<T, RS>(p, s_out, c, tile.tensor_offset + j,
+                                            tile.bucket_offset + j, acc);
                     }
                     continue;
                 }
@@ -107,57 +166,69 @@ __global__ void __launch_bounds__(kThreads, NT > 0 ? 1 : 2)
 #pragma unroll 1
             for (int u = 0; u < U; ++u) {
                 const long long v = v0 + (long long)u * blockDim.x;
-                if (v < nvec) bucket_vector<T, Op>(p, s_in, s_out, c, tile.tensor_offset + v * V);
+                if (v < nvec)
+                    bucket_vector<T, Op, RS>(p, s_in, s_out, c, tile.tensor_offset + v * V,
+                                             tile.bucket_offset + v * V);
             }
         }
         // the tile's tail, or all of it when its addresses are not aligned
-        for (long long j = nvec * V + threadIdx.x; j < tile.count; j += blockDim.x) {
-            const long long i = tile.tensor_offset + j;
-            SharedScalarLoader<T> ld{s_in, i};
-            A val = fold_ring_doubled<Op>(ld, p.n, c).x[0];
-            if (p.avg) val = avg_div(val, p.n);
-            for (int r = 0; r < p.n; ++r) store1(static_cast<T*>(s_out[r]) + i, val);
+        for (long long j = nvec * V + threadIdx.x; j < tile.count; j += blockDim.x)
+            bucket_element<T, Op, RS>(p, s_in, s_out, c, tile.tensor_offset + j,
+                                      tile.bucket_offset + j);
+        if constexpr (RS) {
+            if (t == 0) bucket_fill<T, Op>(p, 0, tile.bucket_offset);
+            bucket_fill<T, Op>(p, tile.bucket_offset + tile.count, next_start);
+        }
+        if (tn < p.ntiles) {
+            tile = next_tile;
+            if (me < p.n) {
+                my_in = p.in[(long long)tile.tensor * p.n + me];
+                if constexpr (!RS) my_out = p.out[(long long)tile.tensor * p.n + me];
+            }
         }
     }
 }
 
 template <class T, class Op, int NT, int U>
-cudaError_t launch_bucket_n(const BucketParams& p, cudaStream_t st) {
+cudaError_t launch_bucket_n(const BucketParams& p, bool rs, cudaStream_t st) {
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
     const int blocks = std::min(p.ntiles, 16 * sms);
-    vc_bucket_ar_kernel<T, Op, NT, U><<<blocks, kThreads, 0, st>>>(p);
+    if (rs)
+        vc_bucket_kernel<T, Op, NT, U, true><<<blocks, kThreads, 0, st>>>(p);
+    else
+        vc_bucket_kernel<T, Op, NT, U, false><<<blocks, kThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 // Compile-time N for the common rank counts (N x U at most 16 vectors of
 // registers per thread), a run-time N otherwise.
 template <class T, class Op>
-cudaError_t launch_bucket_t(const BucketParams& p, cudaStream_t st) {
+cudaError_t launch_bucket_t(const BucketParams& p, bool rs, cudaStream_t st) {
     switch (p.n) {
-    case 2: return launch_bucket_n<T, Op, 2, 4>(p, st);
-    case 4: return launch_bucket_n<T, Op, 4, 4>(p, st);
-    case 8: return launch_bucket_n<T, Op, 8, 2>(p, st);
-    default: return launch_bucket_n<T, Op, 0, 1>(p, st);
+    case 2: return launch_bucket_n<T, Op, 2, 4>(p, rs, st);
+    case 4: return launch_bucket_n<T, Op, 4, 4>(p, rs, st);
+    case 8: return launch_bucket_n<T, Op, 8, 2>(p, rs, st);
+    default: return launch_bucket_n<T, Op, 0, 1>(p, rs, st);
     }
 }
 
 template <class T>
-cudaError_t launch_bucket_op(const BucketParams& p, vc_op_t op, cudaStream_t st) {
+cudaError_t launch_bucket_op(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st) {
     switch (op) {
     case VC_SUM:
-    case VC_AVG: return launch_bucket_t<T, OpSum>(p, st);
-    case VC_PROD: return launch_bucket_t<T, OpProd>(p, st);
-    case VC_MAX: return launch_bucket_t<T, OpMax>(p, st);
-    case VC_MIN: return launch_bucket_t<T, OpMin>(p, st);
+    case VC_AVG: return launch_bucket_t<T, OpSum>(p, rs, st);
+    case VC_PROD: return launch_bucket_t<T, OpProd>(p, rs, st);
+    case VC_MAX: return launch_bucket_t<T, OpMax>(p, rs, st);
+    case VC_MIN: return launch_bucket_t<T, OpMin>(p, rs, st);
     default: return cudaErrorInvalidValue;
     }
 }
 
 // Launchers by element type (vc_bucket_inst.cu).
-cudaError_t launch_bucket_i32(const BucketParams& p, vc_op_t op, cudaStream_t st);
-cudaError_t launch_bucket_i64(const BucketParams& p, vc_op_t op, cudaStream_t st);
-cudaError_t launch_bucket_f32(const BucketParams& p, vc_op_t op, cudaStream_t st);
-cudaError_t launch_bucket_bf16(const BucketParams& p, vc_op_t op, cudaStream_t st);
+cudaError_t launch_bucket_i32(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st);
+cudaError_t launch_bucket_i64(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st);
+cudaError_t launch_bucket_f32(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st);
+cudaError_t launch_bucket_bf16(const BucketParams& p, vc_op_t op, bool rs, cudaStream_t st);
 
 }  // namespace vc

@@ -749,7 +749,8 @@ def bucket_report(torch, vc, args, dev):
     gradients as bucket views (no copy), with packing (three launches per
     bucket) and fused (one launch per bucket, the tensors reduced where they
     are); the per-tensor and bucket loops also replayed from a CUDA graph
-    (launch cost amortised)."""
+    (launch cost amortised); and the buckets' ReduceScatter into per-rank
+    shards (ZeRO), from the views, packed, and fused."""
     from allreduce_reducescatter_allgather_gb300 import bucketing
     n = 8
     shapes = transformer_grad_shapes()
@@ -804,7 +805,17 @@ def bucket_report(torch, vc, args, dev):
 
     graphs = []
 
+    def rs_views():
+        gb.reduce_scatter(op=args.op, order=args.order)
+
+    def rs_packed():
+        gb.reduce_scatter_tensors(op=args.op, order=args.order, fused=False)
+
+    def rs_fused():
+        gb.reduce_scatter_tensors(op=args.op, order=args.order, fused=True)
+
     ar_bytes = 2 * n * total
+    rs_bytes = n * total + total
     out = {"ranks": n, "dtype": "bf16", "tensors": len(shapes), "buckets": len(gb.buckets),
            "bytes_per_rank": total}
     for name, fn, launches in (("per_tensor", per_tensor, len(shapes)),
@@ -817,6 +828,14 @@ def bucket_report(torch, vc, args, dev):
         ms = t_ms(fn)
         out[name] = {"us": round(ms * 1e3, 1), "allreduce_gbs": round(ar_bytes / ms / 1e6, 1),
                      "launches": launches}
+    # ZeRO: the buckets' ReduceScatter into per-rank shards
+    for name, fn, launches in (("rs_bucket_views", rs_views, len(gb.buckets)),
+                               ("rs_bucket_packed", rs_packed, 2 * len(gb.buckets))) + (
+            (("rs_bucket_fused", rs_fused, len(gb.buckets)),) if gb.fused_supported(args.order)
+            else ()):
+        ms = t_ms(fn)
+        out[name] = {"us": round(ms * 1e3, 1),
+                     "reduce_scatter_gbs": round(rs_bytes / ms / 1e6, 1), "launches": launches}
     del grads, gb, singles, graphs
     torch.cuda.empty_cache()
     return out

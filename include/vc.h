@@ -296,6 +296,24 @@ vc_status_t vc_all_reduce_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
                                  int nranks, size_t bucket_count, vc_dtype_t dtype, vc_op_t op,
                                  vc_stream_t stream);
 
+/* The ReduceScatter of the same bucket, as ZeRO does with gradients ("NCCL
+ * 专家课程 07", ZeRO/FSDP 为什么停在 ReduceScatter): rank r receives shard r,
+ * the q = vc_shard_count(bucket_count, nranks) elements from bucket index
+ * r*q, reduced in ring order: the bits vc_reduce_scatter gives on the
+ * packed bucket (the gaps between tensors are zeros, which every op
+ * reduces to zero; positions from bucket_count to nranks*q hold the op's
+ * identity, 0 for AVG).  One launch; the tensors are read where they are.
+ * dev_tiles, dev_sendbufs, bucket_count: as for vc_all_reduce_bucket (the
+ *   tiles in the order vc_bucket_plan wrote them).
+ * recvbufs: HOST array of nranks DEVICE pointers, shard r of q elements,
+ *   pairwise disjoint (checked) and disjoint from the planned tensors (not
+ *   checked: those pointers live in device memory).
+ * ntiles == 0 launches nothing. */
+vc_status_t vc_reduce_scatter_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
+                                     const void *const *dev_sendbufs, void *const *recvbufs,
+                                     int nranks, size_t bucket_count, vc_dtype_t dtype,
+                                     vc_op_t op, vc_stream_t stream);
+
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
  * 32 MiB on every GPU that loads this library, held until the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -56,7 +56,8 @@ def test_header_declares_the_entry_points():
                             "vc_all_reduce", "vc_all_reduce_decomposed", "vc_reduce",
                             "vc_broadcast", "vc_copy_tiles",
                             "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan",
-                            "vc_all_reduce_bucket", "vc_status_string"])
+                            "vc_all_reduce_bucket", "vc_reduce_scatter_bucket",
+                            "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -478,3 +479,21 @@ def test_all_reduce_bucket_checks(vc):
     assert L.vc_all_reduce_bucket((1 << 40) + 4, 5, 1 << 41, 1 << 42, 4, 100, F32, SUM,
                                   None) == INVALID
     assert L.vc_all_reduce_bucket(1 << 40, 5, 1 << 41, 1 << 42, 4, 100, F32, SUM, None) == CUDA
+
+
+def test_reduce_scatter_bucket_checks(vc):
+    L = vc.lib()
+    shards = fake(4, 1 << 43)
+    t = table(vc, shards)
+    assert L.vc_reduce_scatter_bucket(None, 0, None, None, 4, 100, F32, SUM, None) == SUCCESS
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, t, 4, 100, F32, 9, None) == INVALID
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, None, 4, 100, F32, SUM, None) == INVALID
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, t, 4, 0, F32, SUM, None) == INVALID
+    bad = list(shards)
+    bad[2] = 0
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, table(vc, bad), 4, 100, F32, SUM,
+                                      None) == INVALID
+    bad[2] = shards[1] + 40   # q = 25 fp32 = 100 bytes: overlaps shard 1
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, table(vc, bad), 4, 100, F32, SUM,
+                                      None) == ALIAS
+    assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, t, 4, 100, F32, SUM, None) == CUDA

@@ -76,6 +76,20 @@ def _oracle_buckets(gb, grads_np, dtype, op, order):
     return out
 
 
+def _oracle_bucket_shards(gb, grads_np, dtype, op, order):
+    """The oracle's ReduceScatter of every bucket as the library lays it out
+    (zero padding between tensors): shards[bucket][rank]."""
+    st = oracle.NP_STORAGE[dtype]
+    out = []
+    for b in gb.buckets:
+        bufs = [np.zeros(b.count, st) for _ in range(gb.nranks)]
+        for r in range(gb.nranks):
+            for t, off in zip(b.tensors, b.offsets):
+                bufs[r][off:off + gb.numels[t]] = grads_np[r][t]
+        out.append(oracle.reduce_scatter(bufs, dtype, op, order))
+    return out
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype,op,order", [("float32", "sum", "ring"),
                                             ("bfloat16", "avg", "recursive_halving"),
@@ -107,6 +121,33 @@ def test_bucket_views_and_packing_match_oracle(genv, dtype, op, order):
     for r in range(n):
         for t, v in enumerate(gb.views(r)):
             assert_bits_equal(to_host(v.reshape(-1), dtype), want[r][t], dtype, f"view r{r} t{t}")
+    # the buckets' ReduceScatter (ZeRO): from the views' buffers, and from
+    # separately allocated tensors (packed, or fused where the order allows)
+    want_rs = _oracle_bucket_shards(gb, grads_np, dtype, op, order)
+    for r in range(n):  # the AllReduce above overwrote the views
+        for t, v in enumerate(gb.views(r)):
+            v.copy_(to_dev(grads_np[r][t]).view(v.shape))
+    got = gb.reduce_scatter(op=op, order=order)
+    torch.cuda.synchronize()
+    for i, sh in enumerate(got):
+        for r in range(n):
+            assert_bits_equal(to_host(sh[r], dtype), want_rs[i][r], dtype, f"RS views b{i} r{r}")
+    for fused in (False, True):
+        grads = [[to_dev(grads_np[r][t]).view(SHAPES[t]).clone() for t in range(len(SHAPES))]
+                 for r in range(n)]
+        for b in gb.buckets:
+            for buf in b.buffers:
+                buf.zero_()
+        gb.bind(grads)
+        for sh in got:
+            for t in sh:
+                t.fill_(3)
+        got = gb.reduce_scatter_tensors(op=op, order=order, fused=fused)
+        torch.cuda.synchronize()
+        for i, sh in enumerate(got):
+            for r in range(n):
+                assert_bits_equal(to_host(sh[r], dtype), want_rs[i][r], dtype,
+                                  f"RS fused={fused} b{i} r{r}")
     # separately allocated tensors: packed, reduced, unpacked; and fused
     # (one launch per bucket) where the order allows it
     for fused in (False, True):
@@ -179,7 +220,7 @@ def test_fused_bucket_matches_oracle(genv, dtype, op, n):
     ins = [[to_dev(host[r][k], k % 2) for k in range(len(counts))] for r in range(n)]
     outs = [[to_dev(np.zeros_like(host[r][k]), (k + 1) % 2) for k in range(len(counts))]
             for r in range(n)]
-    plan = vc.BucketAllReduce(ins, outs)
+    plan = vc.BucketPlan(ins, outs)
     plan(op=op)
     torch.cuda.synchronize()
     # the oracle: the packed bucket, its ring AllReduce, sliced back
@@ -200,6 +241,15 @@ def test_fused_bucket_matches_oracle(genv, dtype, op, n):
                               f"N={n} rank {r} tensor {k}")
             # inputs untouched (out of place)
             assert_bits_equal(to_host(ins[r][k], dtype), host[r][k], dtype, "input kept")
+    # the bucket's ReduceScatter: every shard element, gaps and padding
+    # included, against the oracle's ReduceScatter of the packed bucket
+    q = plan.shard_count
+    shards = [torch.full((q,), 7, dtype=tdt, device=dev) for _ in range(n)]
+    plan.reduce_scatter(shards, op=op)
+    torch.cuda.synchronize()
+    zs = oracle.reduce_scatter(bufs, dtype, op, "ring")
+    for r in range(n):
+        assert_bits_equal(to_host(shards[r], dtype), zs[r], dtype, f"N={n} shard {r}")
 
 
 @pytest.mark.gpu
