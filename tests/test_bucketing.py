@@ -194,12 +194,14 @@ FUSED_SHAPES = [(5,), (16_381,), (0,), (3, 7), (70_001,), (1,), (4096,), (33_333
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "avg"),
                                       ("int32", "prod"), ("int64", "min")])
-@pytest.mark.parametrize("n", [3, 8, 12])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 12, 64])
 def test_fused_bucket_matches_oracle(genv, dtype, op, n):
     """vc_all_reduce_bucket against the oracle's ring AllReduce of the packed
     bucket (each tensor at the previous one's end rounded up to 16 bytes,
     zeros between), out of place, with every other tensor a view whose base
-    is one element off the 16-byte grid (the element-by-element path)."""
+    is one element off the 16-byte grid (the element-by-element path); N =
+    2, 4, 8 take the compile-time kernels, the others the run-time one.
+    Then vc_reduce_scatter_bucket against the oracle's ReduceScatter."""
     torch, vc, bk, dev = genv
     tdt = {"float32": torch.float32, "bfloat16": torch.bfloat16, "int32": torch.int32,
            "int64": torch.int64}[dtype]
