@@ -438,6 +438,29 @@ def test_edge_shapes(env, dtype, offset):
             check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M} off={offset}")
 
 
+EVERY_N = list(range(1, 18)) + [31, 32, 33, 48, 63, 64]
+
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+def test_every_rank_count(env, dtype):
+    """Every rank count from 1 to 17 and around 32 and 64, in every order it
+    takes: each compile-time instance (ring 1..8, 16, 32, 64; trees 3, 5, 6,
+    7 and the powers of two) and the run-time ones, on the vector path (the
+    length spans many vectors per thread and ends in a ragged tail), every
+    path, every element."""
+    k = 0
+    for n in EVERY_N:
+        M = 3 * 4096 + 17 * n + 5
+        for order in orders_for(n):
+            op = OPS[k % len(OPS)]
+            k += 1
+            xs = gen(dtype, n, M, seed=9000 + 31 * n + k)
+            if op == "prod" and dtype in ("float32", "bfloat16"):
+                xs = gen_prod_floats(dtype, n, M)
+            res = run_all_paths(env, xs, dtype, op, order)
+            check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M}")
+
+
 TREE_N = [3, 5, 6, 7, 9, 12, 17, 24, 33, 48, 63]
 
 
