@@ -847,10 +847,18 @@ def run_sweep(args):
     JSON line per point with RS / AG / fused AR GB/s and their fraction of the
     measured copy peak (SUM, the order given by --order).  Inputs are made on
     the device; each kernel's time is the median of 5 single calls after 3
-    warm-ups.  Before each call a write of twice the L2 evicts the last
+    warm-ups.  Before each call a read of twice the L2 evicts the last
     call's data, and it keeps the GPU busy while the host issues the call:
     the events then time the call on the device, launch latency included,
-    without the host's time to reach the launch."""
+    without the host's time to reach the launch.  (A write would leave the
+    L2 full of dirty lines, up to 126 MB that the timed call would have to
+    write back: measured, that cost N = 2 ReduceScatter at 64 MiB per rank
+    a fifth of its rate.  After a read the lines are clean, and at 256 MiB
+    per rank a single call then measures what the back-to-back bench does.)
+    Points with 64 MiB to 4 GiB of input per call also get "sustained":
+    back-to-back calls over enough buffer sets that every call reads from
+    HBM and meets the previous calls' dirty lines in L2, as in a training
+    loop."""
     import torch
 
     import allreduce_reducescatter_allgather_gb300 as vc
@@ -860,17 +868,18 @@ def run_sweep(args):
     peak, kind = measured_peak()
     stream = torch.cuda.current_stream(dev)
 
-    # a buffer twice the L2: writing it between calls evicts the last call's
+    # a buffer twice the L2: reading it between calls evicts the last call's
     # data, so points whose data would fit in L2 are still timed from HBM
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+    flush = torch.ones(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def t_ms(fn, reps=5):
         for _ in range(3):
             fn()
         times = []
         for _ in range(reps):
-            flush.zero_()
+            torch.sum(flush, dim=0, out=sink)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -878,6 +887,43 @@ def run_sweep(args):
             b.synchronize()
             times.append(a.elapsed_time(b))
         return sorted(times)[len(times) // 2]
+
+    def sustained(n, M, dtype, dist, kw, d, z, b, set_bytes):
+        """Back-to-back calls, the way a training loop issues them: K sets
+        of buffers whose inputs together exceed twice the L2 are taken in
+        turn, so every call reads from HBM and finds the L2 full of the
+        previous calls' dirty lines.  Per-call average over 3 rounds."""
+        K = -(-2 * l2 // set_bytes) + 1
+        sets = [(d, z)]
+        for k in range(1, K):
+            dk = si.generate_device(torch, dtype, dist, n, M, si.SEED_BASE + 40 + k, dev, **kw)
+            sets.append((dk, [torch.empty_like(t) for t in z]))
+        out = {"sets": K}
+        for name, key in (("reduce_scatter", "reduce_scatter"), ("all_gather", "all_gather"),
+                          ("all_reduce", "fused_ar")):
+            calls = []
+            for dk, zk in sets:
+                if name == "reduce_scatter":
+                    calls.append(vc.prepare_reduce_scatter(dk, zk, op=args.op, order=args.order))
+                elif name == "all_gather":
+                    calls.append(vc.prepare_all_gather(zk, dk))
+                else:
+                    calls.append(vc.prepare_all_reduce(dk, None, op=args.op, order=args.order))
+            for c in calls:  # warm-up round
+                c(stream=stream)
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(3):
+                for c in calls:
+                    c(stream=stream)
+            e.record(stream)
+            e.synchronize()
+            ms = a.elapsed_time(e) / (3 * K)
+            g = b[key] / (ms / 1e3) / 1e9
+            out[name] = {"us": round(ms * 1e3, 2), "gbs": round(g, 1), "frac": round(g / peak, 4)}
+        del sets
+        return out
 
     for n, nbytes in si.sweep_points():
         if args.order == "recursive_halving" and n & (n - 1):
@@ -896,7 +942,7 @@ def run_sweep(args):
             b = step_bytes(n, M, es)
             line = {"sweep": "size_x_ranks", "n": n, "bytes_per_rank": nbytes, "dtype": dtype,
                     "op": args.op, "order": args.order, "peak": peak, "peak_kind": kind,
-                    "timing": "median of 5 single calls, each after an L2-evicting write"}
+                    "timing": "median of 5 single calls, each after an L2-evicting read"}
             for name, fn, key in (("reduce_scatter", rs, "reduce_scatter"),
                                   ("all_gather", ag, "all_gather"),
                                   ("all_reduce", ar, "fused_ar")):
@@ -904,6 +950,9 @@ def run_sweep(args):
                 g = b[key] / (ms / 1e3) / 1e9
                 line[name] = {"us": round(ms * 1e3, 2), "gbs": round(g, 1),
                               "frac": round(g / peak, 4)}
+            set_bytes = n * nbytes
+            if 64 << 20 <= set_bytes <= 4 << 30:
+                line["sustained"] = sustained(n, M, dtype, dist, kw, d, z, b, set_bytes)
             print(json.dumps(line), flush=True)
             del d, z, rs, ag, ar
             torch.cuda.empty_cache()

@@ -181,10 +181,17 @@ WORKLOADS = {
 }
 
 
+# The smallest per-rank size at which the fused AllReduce and the
+# ReduceScatter are to hold 80 % of the copy peak; the sweep measures it too,
+# although 8 KiB * 4^k steps over it.
+TARGET_BYTES_PER_RANK = 64 << 20
+
+
 def sweep_points(max_total_bytes: int = 64 << 30):
     """The size x rank-count sweep: per-rank bytes 8 KiB * 4^k (k = 0..8) and
-    1 GiB, N in {2, 4, 8, 16, 64}, keeping N * bytes <= 64 GiB."""
-    sizes = [8192 * 4 ** k for k in range(9)] + [1 << 30]
+    1 GiB, plus the 64 MiB target point, N in {2, 4, 8, 16, 64}, keeping
+    N * bytes <= 64 GiB."""
+    sizes = sorted([8192 * 4 ** k for k in range(9)] + [TARGET_BYTES_PER_RANK, 1 << 30])
     pts = []
     for nbytes in sizes:
         for n in (2, 4, 8, 16, 64):
