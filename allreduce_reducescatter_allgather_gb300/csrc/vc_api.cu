@@ -238,27 +238,17 @@ cudaError_t launch_gather(const GatherParams& p_in, int esize, cudaStream_t st) 
     int groups = 1;
     while ((long long)blocks * groups < target && p.n / (groups * 2) >= 4) groups *= 2;
     p.rpg = (p.n + groups - 1) / groups;
-    // Programmatic dependent launch: the gather may be scheduled while the
-    // preceding kernel drains; it waits on griddepcontrol before any access.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks, groups);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // programmatic dependent launch: the gather may be scheduled while the
+    // preceding kernel drains; it waits on griddepcontrol before any access
+    const dim3 grid(blocks, groups);
     cudaError_t e;
     switch (esize) {
-    case 2: e = cudaLaunchKernelEx(&cfg, vc_ag_kernel<2>, p); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, vc_ag_kernel<4>, p); break;
-    case 8: e = cudaLaunchKernelEx(&cfg, vc_ag_kernel<8>, p); break;
+    case 2: e = launch_pdl(vc_ag_kernel<2>, grid, dim3(kThreads), st, p); break;
+    case 4: e = launch_pdl(vc_ag_kernel<4>, grid, dim3(kThreads), st, p); break;
+    case 8: e = launch_pdl(vc_ag_kernel<8>, grid, dim3(kThreads), st, p); break;
     default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace vc

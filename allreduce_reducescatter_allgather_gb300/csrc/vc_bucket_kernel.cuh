@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     // already fetched tile t + gridDim.x's descriptor and (threads r < N)
     // that tile's pointers, so a new tile starts after one shared-memory
     // round trip instead of a chain of dependent global loads.
+    // launched with programmatic stream serialization: wait for the kernel
+    // before this one to complete (and its writes to be visible) first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int t = blockIdx.x;
     if (t >= p.ntiles) return;
     vc_bucket_tile_t tile = p.tiles[t];
@@ -187,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     }
+    // this block is done: a kernel launched after this one may start
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <class T, class Op, int NT, int U>
@@ -194,11 +199,8 @@ cudaError_t launch_bucket_n(const BucketParams& p, bool rs, cudaStream_t st) {
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
     const int blocks = std::min(p.ntiles, 16 * sms);
-    if (rs)
-        vc_bucket_kernel<T, Op, NT, U, true><<<blocks, kThreads, 0, st>>>(p);
-    else
-        vc_bucket_kernel<T, Op, NT, U, false><<<blocks, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    if (rs) return launch_pdl(vc_bucket_kernel<T, Op, NT, U, true>, dim3(blocks), dim3(kThreads), st, p);
+    return launch_pdl(vc_bucket_kernel<T, Op, NT, U, false>, dim3(blocks), dim3(kThreads), st, p);
 }
 
 // Compile-time N for the common rank counts (N x U at most 16 vectors of

@@ -12,6 +12,9 @@ namespace {
 __global__ void __launch_bounds__(kThreads) vc_copy_tiles_kernel(const vc_copy_tile_t* tiles,
                                                                   int ntiles) {
     constexpr int S = 4;
+    // launched with programmatic stream serialization: wait for the kernel
+    // before this one to complete (and its writes to be visible) first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const vc_copy_tile_t tile = tiles[t];
         const unsigned char* src = static_cast<const unsigned char*>(tile.src);
@@ -43,6 +46,8 @@ __global__ void __launch_bounds__(kThreads) vc_copy_tiles_kernel(const vc_copy_t
             for (size_t k = threadIdx.x; k < bytes; k += blockDim.x) dst[k] = src[k];
         }
     }
+    // this block is done: a kernel launched after this one may start
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace
@@ -60,7 +65,7 @@ extern "C" vc_status_t vc_copy_tiles(const vc_copy_tile_t* dev_tiles, int ntiles
     if (hook != nullptr && hook[0] != '\0' && hook[0] != '0') return VC_ERR_CUDA;
     const int blocks = grid_blocks((long long)ntiles * kThreads);
     if (blocks < 1) return VC_ERR_CUDA;
-    vc_copy_tiles_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(dev_tiles,
-                                                                                   ntiles);
-    return cudaGetLastError() == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
+    const cudaError_t e = launch_pdl(vc_copy_tiles_kernel, dim3(blocks), dim3(kThreads),
+                                     static_cast<cudaStream_t>(stream), dev_tiles, ntiles);
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
 }

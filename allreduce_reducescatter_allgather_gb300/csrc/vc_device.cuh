@@ -794,6 +794,12 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
 template <class T, class Op, int ORDER, int NT, int U, bool RS>
 __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
     constexpr int V = Traits<T>::V;
+    // Launched with programmatic stream serialization, this grid may be
+    // scheduled while the kernel before it drains; wait for that kernel to
+    // complete and its writes to be visible before touching global memory.
+    // (After a kernel that never signals, or launched plainly, this returns
+    // once that kernel has completed, or at once.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr bool kPre = (NT > 0 && NT <= 8);
     // ring beyond 8 ranks: rotated rank indices read from shared memory
     // (with a run-time N, a doubled input table: entry k is rank k mod N)
@@ -1000,6 +1006,30 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
             }
         }
     }
+    // this block is done: a kernel launched after this one may start
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` with programmatic stream serialization: its grid may be
+// scheduled while the kernel before it on the stream drains.  Every kernel
+// launched this way executes griddepcontrol.wait before its first global
+// access, so it still sees all of the preceding kernel's writes.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 // Launchers by element type (vc_reduce_dispatch.cu, which picks the slice of

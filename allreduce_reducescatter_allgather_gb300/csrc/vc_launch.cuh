@@ -7,17 +7,19 @@
 
 namespace vc {
 
+// Programmatic dependent launch (launch_pdl): the grid may be scheduled
+// while the kernel before it on the stream drains (the kernels wait on
+// griddepcontrol before their first global access, and signal their
+// dependents as each block finishes), so back-to-back collectives do not pay
+// the full launch gap.
 template <class T, class Op, int ORDER, int NT, int U>
 cudaError_t launch_one(const ReduceParams& p, bool rs, cudaStream_t st) {
     constexpr int V = Traits<T>::V;
     const long long nvec = (p.limit + V - 1) / V;
     const int blocks = grid_blocks((nvec + U - 1) / U);
     if (blocks < 1) return cudaErrorInvalidConfiguration;
-    if (rs)
-        vc_rs_kernel<T, Op, ORDER, NT, U><<<blocks, kThreads, 0, st>>>(p);
-    else
-        vc_ar_kernel<T, Op, ORDER, NT, U><<<blocks, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    if (rs) return launch_pdl(vc_rs_kernel<T, Op, ORDER, NT, U>, dim3(blocks), dim3(kThreads), st, p);
+    return launch_pdl(vc_ar_kernel<T, Op, ORDER, NT, U>, dim3(blocks), dim3(kThreads), st, p);
 }
 
 // Up to N = 8 a thread holds all N operands of U vectors in registers (N*U
