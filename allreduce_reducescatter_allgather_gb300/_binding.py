@@ -30,7 +30,7 @@ MAX_RANKS = 64
 EXPORTS = ("vc_shard_count", "vc_reduce_scatter", "vc_all_gather", "vc_all_reduce",
            "vc_all_reduce_decomposed", "vc_reduce", "vc_broadcast", "vc_copy_tiles",
            "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan", "vc_all_reduce_bucket",
-           "vc_reduce_scatter_bucket", "vc_status_string")
+           "vc_reduce_scatter_bucket", "vc_all_gather_bucket", "vc_status_string")
 
 
 class BucketTile(ctypes.Structure):
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(sz)]
         L.vc_all_reduce_bucket.argtypes = [vp, i32, vp, vp, i32, sz, i32, i32, vp]
         L.vc_reduce_scatter_bucket.argtypes = [vp, i32, vp, vpp, i32, sz, i32, i32, vp]
+        L.vc_all_gather_bucket.argtypes = [vp, i32, vpp, vp, i32, sz, i32, vp]
+        L.vc_all_gather_bucket.restype = i32
         L.vc_bucket_plan.restype = i32
         L.vc_all_reduce_bucket.restype = i32
         L.vc_reduce_scatter_bucket.restype = i32
@@ -391,7 +393,8 @@ class BucketPlan:
     on a 16-byte boundary.  all_reduce() (also the call operator) gives every
     element the bits the ring-order AllReduce of that bucket gives it;
     reduce_scatter() writes shard r of the bucket's ring-order ReduceScatter
-    to rank r's shard.  Planned once (pointer checks, aliasing, tiles); each
+    to rank r's shard; all_gather() writes the shards back into every rank's
+    output tensors.  Planned once (pointer checks, aliasing, tiles); each
     call is one launch.  The plan keeps the tensors' addresses: make a new
     one if they change."""
 
@@ -442,6 +445,23 @@ class BucketPlan:
         self._checked_shards = None
         self.host_tiles = tiles
 
+    def _check_shards(self, shards):
+        """One shard per rank, of the bucket's dtype, device and shard length,
+        overlapping no planned tensor (checked once per set of buffers)."""
+        if len(shards) != self.nranks:
+            raise ValueError("one shard per rank")
+        key = tuple(t.data_ptr() for t in shards)
+        if key == self._checked_shards:
+            return
+        _check_tensors("shards", shards, self.dtype, self.shard_count, self.device)
+        for t in shards:
+            for rows in self._keep:
+                for row in rows:
+                    for g in row:
+                        if g.numel() and _overlaps(t, g):
+                            raise ValueError("a shard overlaps a bucket tensor")
+        self._checked_shards = key
+
     @property
     def shard_count(self) -> int:
         """q: the elements of one rank's shard of the bucket."""
@@ -453,21 +473,21 @@ class BucketPlan:
     def reduce_scatter(self, shards, op: str = "sum", stream=None):
         """shards[r]: rank r's output, shard_count elements of the bucket's
         dtype on its device; disjoint from each other and from the tensors."""
-        if len(shards) != self.nranks:
-            raise ValueError("one shard per rank")
-        key = tuple(t.data_ptr() for t in shards)
-        if key != self._checked_shards:  # checked once per set of shard buffers
-            _check_tensors("shards", shards, self.dtype, self.shard_count, self.device)
-            for t in shards:
-                for row in self._keep[0]:
-                    for g in row:
-                        if g.numel() and _overlaps(t, g):
-                            raise ValueError("a shard overlaps a bucket tensor")
-            self._checked_shards = key
+        self._check_shards(shards)
         check_status(lib().vc_reduce_scatter_bucket(
             ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
             ctypes.c_void_p(self.in_ptrs.data_ptr()), _ptrs(shards), self.nranks,
             self.bucket_count, DTYPES[self.dtype], OPS[op], _stream(stream, self.device)))
+
+    def all_gather(self, shards, stream=None):
+        """shards[r] (shard_count elements) gathered back into every rank's
+        output tensors: out[r][k] receives the bucket's elements of tensor k
+        from the shards that hold them."""
+        self._check_shards(shards)
+        check_status(lib().vc_all_gather_bucket(
+            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles, _ptrs(shards),
+            ctypes.c_void_p(self.out_ptrs.data_ptr()), self.nranks, self.bucket_count,
+            DTYPES[self.dtype], _stream(stream, self.device)))
 
     def all_reduce(self, op: str = "sum", stream=None):
         check_status(lib().vc_all_reduce_bucket(

@@ -224,6 +224,17 @@ class GradientBuckets:
             _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.unpack_tiles.data_ptr()),
                                                   b.ntiles, s))
 
+    def all_gather_tensors(self, stream=None):
+        """FSDP's unpack: every bucket's shards (shards(bucket), e.g. after
+        the optimizer updated them) gathered back into the bound tensors of
+        every rank, one launch per bucket.  After reduce_scatter_tensors it
+        completes the decomposed AllReduce of the buckets."""
+        torch = self.torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        for i, b in enumerate(self.buckets):
+            b.fused.all_gather(self.shards(i), stream=stream)
+
     def reduce_scatter_tensors(self, op: str = "sum", order: str = "ring", stream=None,
                                fused: bool = True):
         """For the bound tensors: the bucket's ReduceScatter into

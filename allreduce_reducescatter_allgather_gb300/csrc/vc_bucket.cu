@@ -27,6 +27,61 @@
 namespace vc {
 namespace {
 
+// AllGather of the bucket: tile by tile, the shard of the tile's chunk
+// (one read) into every rank's output tensor (N writes).  Moves bits only,
+// so it is typed by element size.  Same software-pipelined tile set-up as
+// the reduction kernel; a thread copies up to 4 vectors per round, all
+// loaded before any is stored.
+template <int ES>
+__global__ void __launch_bounds__(kThreads) vc_bucket_gather_kernel(const __grid_constant__ BucketParams p) {
+    using U = typename Bits<ES>::U;
+    constexpr int V = 16 / ES;
+    constexpr int S = 4;
+    __shared__ void* s_out[kMaxRanks];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int t = blockIdx.x;
+    if (t >= p.ntiles) return;
+    vc_bucket_tile_t tile = p.tiles[t];
+    const int me = threadIdx.x;
+    void* my_out = me < p.n ? p.out[(long long)tile.tensor * p.n + me] : nullptr;
+    for (; t < p.ntiles; t += gridDim.x) {
+        __syncthreads();  // the last tile's writers are done with the table
+        if (me < p.n) s_out[me] = my_out;
+        __syncthreads();
+        const int tn = t + gridDim.x;
+        vc_bucket_tile_t next_tile = tile;
+        if (tn < p.ntiles) next_tile = p.tiles[tn];
+        const int c = (int)(tile.bucket_offset / p.q);
+        const U* src = static_cast<const U*>(p.shard[c]) + (tile.bucket_offset - (long long)c * p.q);
+        const long long nvec = (tile.flags & 1) ? tile.count / V : 0;
+        for (long long v0 = threadIdx.x; v0 < nvec; v0 += (long long)blockDim.x * S) {
+            uint4 val[S];
+#pragma unroll
+            for (int u = 0; u < S; ++u) {
+                const long long v = v0 + (long long)u * blockDim.x;
+                if (v < nvec) val[u] = ld_aligned<ES>(src + v * V);
+            }
+            for (int r = 0; r < p.n; ++r) {
+                U* dst = static_cast<U*>(s_out[r]) + tile.tensor_offset;
+#pragma unroll
+                for (int u = 0; u < S; ++u) {
+                    const long long v = v0 + (long long)u * blockDim.x;
+                    if (v < nvec) st16(dst + v * V, val[u]);
+                }
+            }
+        }
+        for (long long j = nvec * V + threadIdx.x; j < tile.count; j += blockDim.x) {
+            const U x = src[j];
+            for (int r = 0; r < p.n; ++r) static_cast<U*>(s_out[r])[tile.tensor_offset + j] = x;
+        }
+        if (tn < p.ntiles) {
+            tile = next_tile;
+            if (me < p.n) my_out = p.out[(long long)tile.tensor * p.n + me];
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 int esize(vc_dtype_t dt) {
     switch (dt) {
     case VC_INT32: return 4;
@@ -228,4 +283,45 @@ extern "C" vc_status_t vc_reduce_scatter_bucket(const vc_bucket_tile_t* dev_tile
     p.n = nranks;
     p.avg = op == VC_AVG;
     return launch_bucket(p, dtype, op, true, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" vc_status_t vc_all_gather_bucket(const vc_bucket_tile_t* dev_tiles, int ntiles,
+                                            const void* const* sendbufs, void* const* dev_recvbufs,
+                                            int nranks, size_t bucket_count, vc_dtype_t dtype,
+                                            vc_stream_t stream) {
+    if (nranks < 1 || nranks > VC_MAX_RANKS || ntiles < 0) return VC_ERR_INVALID_ARGUMENT;
+    const int es = esize(dtype);
+    if (es == 0) return VC_ERR_INVALID_ARGUMENT;
+    if (ntiles == 0) return VC_SUCCESS;
+    if (dev_tiles == nullptr || sendbufs == nullptr || dev_recvbufs == nullptr ||
+        bucket_count == 0)
+        return VC_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(dev_tiles) % 8 != 0) return VC_ERR_INVALID_ARGUMENT;
+    const unsigned long long q = (bucket_count + nranks - 1) / nranks;
+    if (q > (1ULL << 62) / (unsigned long long)es) return VC_ERR_INVALID_ARGUMENT;
+    for (int r = 0; r < nranks; ++r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(sendbufs[r]);
+        if (a == 0 || a % es != 0) return VC_ERR_INVALID_ARGUMENT;
+    }
+    if (launch_failure_injected()) return VC_ERR_CUDA;
+    BucketParams p = {};
+    p.tiles = dev_tiles;
+    p.in = nullptr;
+    p.out = dev_recvbufs;
+    for (int r = 0; r < nranks; ++r) p.shard[r] = const_cast<void*>(sendbufs[r]);
+    p.q = (long long)q;
+    p.bucket_count = (long long)bucket_count;
+    p.ntiles = ntiles;
+    p.n = nranks;
+    const int sms = sm_count();
+    if (sms < 1) return VC_ERR_CUDA;
+    const dim3 grid(std::min(ntiles, 16 * sms));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (es) {
+    case 2: e = launch_pdl(vc_bucket_gather_kernel<2>, grid, dim3(kThreads), st, p); break;
+    case 4: e = launch_pdl(vc_bucket_gather_kernel<4>, grid, dim3(kThreads), st, p); break;
+    default: e = launch_pdl(vc_bucket_gather_kernel<8>, grid, dim3(kThreads), st, p); break;
+    }
+    return e == cudaSuccess ? VC_SUCCESS : VC_ERR_CUDA;
 }

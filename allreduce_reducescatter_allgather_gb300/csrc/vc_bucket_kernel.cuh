@@ -2,8 +2,9 @@
 // gradient tensors reduced where they are, in ring order with the ring chunk
 // of their place in the bucket, and written either back to the N ranks'
 // output tensors (AllReduce) or to the shard that owns the chunk
-// (ReduceScatter).  Included by vc_bucket_inst.cu, which the build compiles
-// once per element type.
+// (ReduceScatter).  (The AllGather of the shards back into the tensors moves
+// bits only; its kernel is in vc_bucket.cu.)  Included by vc_bucket_inst.cu,
+// which the build compiles once per element type.
 #pragma once
 
 #include <algorithm>
@@ -15,9 +16,9 @@ namespace vc {
 
 struct BucketParams {
     const vc_bucket_tile_t* tiles;
-    const void* const* in;   // [tensor * n + rank]
-    void* const* out;        // AllReduce outputs, [tensor * n + rank]
-    void* shard[kMaxRanks];  // ReduceScatter outputs: shard r, q elements
+    const void* const* in;   // reduction inputs, [tensor * n + rank]
+    void* const* out;        // AllReduce / AllGather outputs, [tensor * n + rank]
+    void* shard[kMaxRanks];  // shard r, q elements: ReduceScatter output, AllGather input
     long long q;             // ring chunk of the bucket: ceil(bucket_count / n)
     long long bucket_count;
     int ntiles;

@@ -749,8 +749,9 @@ def bucket_report(torch, vc, args, dev):
     gradients as bucket views (no copy), with packing (three launches per
     bucket) and fused (one launch per bucket, the tensors reduced where they
     are); the per-tensor and bucket loops also replayed from a CUDA graph
-    (launch cost amortised); and the buckets' ReduceScatter into per-rank
-    shards (ZeRO), from the views, packed, and fused."""
+    (launch cost amortised); the buckets' ReduceScatter into per-rank
+    shards (ZeRO), from the views, packed, and fused; and the fused
+    AllGather of the shards back into the tensors (FSDP's unpack)."""
     from allreduce_reducescatter_allgather_gb300 import bucketing
     n = 8
     shapes = transformer_grad_shapes()
@@ -814,6 +815,9 @@ def bucket_report(torch, vc, args, dev):
     def rs_fused():
         gb.reduce_scatter_tensors(op=args.op, order=args.order, fused=True)
 
+    def ag_fused():
+        gb.all_gather_tensors()
+
     ar_bytes = 2 * n * total
     rs_bytes = n * total + total
     out = {"ranks": n, "dtype": "bf16", "tensors": len(shapes), "buckets": len(gb.buckets),
@@ -836,6 +840,12 @@ def bucket_report(torch, vc, args, dev):
         ms = t_ms(fn)
         out[name] = {"us": round(ms * 1e3, 1),
                      "reduce_scatter_gbs": round(rs_bytes / ms / 1e6, 1), "launches": launches}
+    # FSDP's unpack: the shards gathered back into the tensors
+    gb.reduce_scatter(op=args.op, order=args.order)
+    ms = t_ms(ag_fused)
+    out["ag_bucket_fused"] = {"us": round(ms * 1e3, 1),
+                              "all_gather_gbs": round(rs_bytes / ms / 1e6, 1),
+                              "launches": len(gb.buckets)}
     del grads, gb, singles, graphs
     torch.cuda.empty_cache()
     return out

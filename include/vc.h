@@ -314,6 +314,24 @@ vc_status_t vc_reduce_scatter_bucket(const vc_bucket_tile_t *dev_tiles, int ntil
                                      int nranks, size_t bucket_count, vc_dtype_t dtype,
                                      vc_op_t op, vc_stream_t stream);
 
+/* The AllGather of the bucket's shards back into the tensors (FSDP's
+ * unpack; after vc_reduce_scatter_bucket it completes the decomposed
+ * AllReduce of the bucket, with the bits of vc_all_reduce_bucket): element
+ * j of tensor k, at bucket index b = b_k + j, receives element b - c*q of
+ * shard c = floor(b / q) on every rank.  One launch.
+ * dev_tiles, bucket_count: from vc_bucket_plan, planned with the output
+ *   tensors (as both sendbufs and recvbufs, or as recvbufs).
+ * sendbufs: HOST array of nranks DEVICE pointers, shard r of
+ *   q = vc_shard_count(bucket_count, nranks) elements.
+ * dev_recvbufs: DEVICE array of the planned output pointer table
+ *   ([k * nranks + r]).
+ * The shards must not overlap the output tensors (not checked: those
+ * pointers live in device memory).  ntiles == 0 launches nothing. */
+vc_status_t vc_all_gather_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
+                                 const void *const *sendbufs, void *const *dev_recvbufs,
+                                 int nranks, size_t bucket_count, vc_dtype_t dtype,
+                                 vc_stream_t stream);
+
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
  * 32 MiB on every GPU that loads this library, held until the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)

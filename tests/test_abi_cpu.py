@@ -57,7 +57,7 @@ def test_header_declares_the_entry_points():
                             "vc_broadcast", "vc_copy_tiles",
                             "vc_all_reduce_decomposed_noalloc", "vc_bucket_plan",
                             "vc_all_reduce_bucket", "vc_reduce_scatter_bucket",
-                            "vc_status_string"])
+                            "vc_all_gather_bucket", "vc_status_string"])
 
 
 def test_library_exports_every_declared_symbol(vc):
@@ -497,3 +497,15 @@ def test_reduce_scatter_bucket_checks(vc):
     assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, table(vc, bad), 4, 100, F32, SUM,
                                       None) == ALIAS
     assert L.vc_reduce_scatter_bucket(1 << 40, 5, 1 << 41, t, 4, 100, F32, SUM, None) == CUDA
+
+
+def test_all_gather_bucket_checks(vc):
+    L = vc.lib()
+    t = table(vc, fake(4, 1 << 43))
+    assert L.vc_all_gather_bucket(None, 0, None, None, 4, 100, F32, None) == SUCCESS
+    assert L.vc_all_gather_bucket(1 << 40, 5, t, 1 << 42, 4, 100, 7, None) == INVALID
+    assert L.vc_all_gather_bucket(1 << 40, 5, None, 1 << 42, 4, 100, F32, None) == INVALID
+    assert L.vc_all_gather_bucket(1 << 40, 5, t, 1 << 42, 65, 100, F32, None) == INVALID
+    assert L.vc_all_gather_bucket(1 << 40, 5, table(vc, [1 << 43, 0, 1 << 44, 1 << 45]),
+                                  1 << 42, 4, 100, F32, None) == INVALID
+    assert L.vc_all_gather_bucket(1 << 40, 5, t, 1 << 42, 4, 100, F32, None) == CUDA

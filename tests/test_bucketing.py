@@ -148,6 +148,14 @@ def test_bucket_views_and_packing_match_oracle(genv, dtype, op, order):
             for r in range(n):
                 assert_bits_equal(to_host(sh[r], dtype), want_rs[i][r], dtype,
                                   f"RS fused={fused} b{i} r{r}")
+        # gathering the shards back into the tensors completes the
+        # decomposed AllReduce of the buckets
+        gb.all_gather_tensors()
+        torch.cuda.synchronize()
+        for r in range(n):
+            for t in range(len(SHAPES)):
+                assert_bits_equal(to_host(grads[r][t].reshape(-1), dtype), want[r][t], dtype,
+                                  f"RS+AG fused={fused} r{r} t{t}")
     # separately allocated tensors: packed, reduced, unpacked; and fused
     # (one launch per bucket) where the order allows it
     for fused in (False, True):
@@ -252,6 +260,25 @@ def test_fused_bucket_matches_oracle(genv, dtype, op, n):
     zs = oracle.reduce_scatter(bufs, dtype, op, "ring")
     for r in range(n):
         assert_bits_equal(to_host(shards[r], dtype), zs[r], dtype, f"N={n} shard {r}")
+    # the bucket's AllGather: those shards back into the output tensors is
+    # the AllReduce again; arbitrary shards give the oracle's AllGather
+    for t in (x for row in outs for x in row):
+        t.fill_(5)
+    plan.all_gather(shards)
+    torch.cuda.synchronize()
+    for r in range(n):
+        for k, c in enumerate(counts):
+            assert_bits_equal(to_host(outs[r][k], dtype), ys[r][base[k]:base[k] + c], dtype,
+                              f"AG(RS) N={n} rank {r} tensor {k}")
+    rnd = [si.generate_rank(dtype, dist, 90, r, q, **kw) for r in range(n)]
+    dsh = [to_dev(a, 0) for a in rnd]
+    plan.all_gather(dsh)
+    torch.cuda.synchronize()
+    gs = oracle.all_gather(rnd, off, dtype)
+    for r in range(n):
+        for k, c in enumerate(counts):
+            assert_bits_equal(to_host(outs[r][k], dtype), gs[r][base[k]:base[k] + c], dtype,
+                              f"AG N={n} rank {r} tensor {k}")
 
 
 @pytest.mark.gpu
