@@ -301,3 +301,34 @@ def test_fused_bucket_in_place_equals_bucket_views(genv):
     for r in range(n):
         for t, v in enumerate(gb.views(r)):
             assert torch.equal(grads[r][t], v)
+
+
+@pytest.mark.gpu
+def test_fused_buckets_replay_from_a_cuda_graph(genv):
+    """The fused bucket calls only enqueue work on the current stream, so a
+    training step can capture them in a CUDA graph once and replay it on new
+    gradients written into the same tensors: every replay gives the bits of
+    the bucket views path on those gradients."""
+    torch, vc, bk, dev = genv
+    n = 4
+    shapes = [(1000, 3), (4096,), (333, 77), (7,)]
+    gb = bk.GradientBuckets(shapes, torch.float32, n, dev, first_cap=64 << 10, cap=1 << 20)
+    grads = [[torch.empty(s, device=dev) for s in shapes] for _ in range(n)]
+    gb.bind(grads)
+    gb.all_reduce_tensors(fused=True)  # first call outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gb.all_reduce_tensors(fused=True)
+    for it in range(3):
+        src = [[torch.randn(s, device=dev) for s in shapes] for _ in range(n)]
+        for r in range(n):
+            for t in range(len(shapes)):
+                grads[r][t].copy_(src[r][t])
+                gb.views(r)[t].copy_(src[r][t])
+        g.replay()
+        gb.all_reduce(op="sum", order="ring")
+        torch.cuda.synchronize()
+        for r in range(n):
+            for t, v in enumerate(gb.views(r)):
+                assert torch.equal(grads[r][t], v), (it, r, t)
