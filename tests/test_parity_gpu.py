@@ -797,3 +797,46 @@ def test_more_than_2_31_elements_per_rank(env, n):
     _check_sampled(env, d, y[0], z, "bfloat16", "sum", "ring", K=1 << 16, seed=31)
     del d, y, z
     torch.cuda.empty_cache()
+
+
+def test_concurrent_host_threads(env):
+    """Every entry point is thread-safe: four host threads, each on its own
+    stream with its own buffers (different N, dtype and order), issue
+    collectives at once; every result matches the oracle."""
+    import threading
+    vc, torch = env.vc, env.torch
+    cases = [(4, "float32", "ring"), (6, "bfloat16", "pairwise_tree"),
+             (8, "int64", "double_binary_tree"), (12, "float32", "ring")]
+    inputs = {k: gen(dt, n, 50_003, seed=600 + k) for k, (n, dt, _) in enumerate(cases)}
+    results, errors = {}, []
+
+    def work(k):
+        try:
+            n, dt, order = cases[k]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                d = to_device(torch, inputs[k], dt, env.dev)
+                y = [torch.empty_like(t) for t in d]
+                q = vc.vc_shard_count(50_003, n)
+                z = [torch.empty(q, dtype=d[0].dtype, device=env.dev) for _ in range(n)]
+                for _ in range(20):
+                    vc.vc_all_reduce(d, y, op="sum", order=order, stream=s)
+                    vc.vc_reduce_scatter(d, z, op="sum", order=order, stream=s)
+            s.synchronize()
+            results[k] = ([to_host(t, dt) for t in y], [to_host(t, dt) for t in z])
+        except Exception as e:  # reported below, on the main thread
+            errors.append((k, e))
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k, (n, dt, order) in enumerate(cases):
+        oy = oracle.all_reduce(inputs[k], dt, "sum", order)
+        oz = oracle.reduce_scatter(inputs[k], dt, "sum", order)
+        ys, zs = results[k]
+        for r in range(n):
+            assert_bits_equal(ys[r], oy[r], dt, f"thread {k} AR rank {r}")
+            assert_bits_equal(zs[r], oz[r], dt, f"thread {k} RS rank {r}")
