@@ -139,6 +139,27 @@ def _check_tensors(name: str, ts, dtype: str, numel: int, device):
             raise ValueError(f"{name}[{r}] holds {t.numel()} elements, expected {numel}")
 
 
+class _OnDevice:
+    """Makes `device` the current CUDA device for one library call, and
+    restores the caller's afterwards (the library launches on the current
+    device).  Costs one query when it is already current."""
+    __slots__ = ("index", "prev")
+
+    def __init__(self, device):
+        self.index = device.index
+
+    def __enter__(self):
+        cuda = _torch().cuda
+        self.prev = cuda.current_device()
+        if self.index is not None and self.prev != self.index:
+            cuda.set_device(self.index)
+
+    def __exit__(self, *exc):
+        if self.index is not None and self.prev != self.index:
+            _torch().cuda.set_device(self.prev)
+        return False
+
+
 def _stream(stream, device):
     torch = _torch()
     if stream is None:
@@ -171,8 +192,9 @@ def vc_reduce_scatter(sendbufs, recvbufs, op: str = "sum", order: str = "ring", 
             f"output shard must hold ceil(M/N) = {q} elements (M = {M}, N = {n}); "
             f"input must be N times the (padded) output size")
     _check_tensors("recvbufs", recvbufs, dt, q, dev)
-    check_status(lib().vc_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
-                                         OPS[op], ORDERS[order], _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                             OPS[op], ORDERS[order], _stream(stream, dev)))
 
 
 def vc_all_gather(sendbufs, recvbufs, count: int | None = None, stream=None):
@@ -189,8 +211,9 @@ def vc_all_gather(sendbufs, recvbufs, count: int | None = None, stream=None):
     if any(t.numel() != q for t in sendbufs):
         raise ValueError(f"input shard must hold ceil(M/N) = {q} elements (M = {M}, N = {n})")
     _check_tensors("sendbufs", sendbufs, dt, q, dev)
-    check_status(lib().vc_all_gather(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
-                                     _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_all_gather(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                         _stream(stream, dev)))
 
 
 def vc_all_reduce(sendbufs, recvbufs=None, op: str = "sum", order: str = "ring", stream=None):
@@ -205,8 +228,9 @@ def vc_all_reduce(sendbufs, recvbufs=None, op: str = "sum", order: str = "ring",
     dev = sendbufs[0].device
     _check_tensors("sendbufs", sendbufs, dt, M, dev)
     _check_tensors("recvbufs", recvbufs, dt, M, dev)
-    check_status(lib().vc_all_reduce(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
-                                     OPS[op], ORDERS[order], _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_all_reduce(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt],
+                                         OPS[op], ORDERS[order], _stream(stream, dev)))
 
 
 def vc_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum",
@@ -226,9 +250,10 @@ def vc_all_reduce_decomposed(sendbufs, shardbufs, recvbufs=None, op: str = "sum"
     if any(t.numel() != q for t in shardbufs):
         raise ValueError(f"shard buffers must hold ceil(M/N) = {q} elements")
     _check_tensors("shardbufs", shardbufs, dt, q, dev)
-    check_status(lib().vc_all_reduce_decomposed(_ptrs(sendbufs), _ptrs(shardbufs),
-                                                _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
-                                                ORDERS[order], _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_all_reduce_decomposed(_ptrs(sendbufs), _ptrs(shardbufs),
+                                                    _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op],
+                                                    ORDERS[order], _stream(stream, dev)))
 
 
 def vc_reduce(sendbufs, recvbuf, op: str = "sum", order: str = "ring", stream=None):
@@ -240,8 +265,9 @@ def vc_reduce(sendbufs, recvbuf, op: str = "sum", order: str = "ring", stream=No
     dev = sendbufs[0].device
     _check_tensors("sendbufs", sendbufs, dt, M, dev)
     _check_tensors("recvbuf", [recvbuf], dt, M, dev)
-    check_status(lib().vc_reduce(_ptrs(sendbufs), ctypes.c_void_p(recvbuf.data_ptr()), n, M,
-                                 DTYPES[dt], OPS[op], ORDERS[order], _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_reduce(_ptrs(sendbufs), ctypes.c_void_p(recvbuf.data_ptr()), n, M,
+                                     DTYPES[dt], OPS[op], ORDERS[order], _stream(stream, dev)))
 
 
 def vc_broadcast(sendbuf, recvbufs, stream=None):
@@ -252,8 +278,9 @@ def vc_broadcast(sendbuf, recvbufs, stream=None):
     dev = sendbuf.device
     _check_tensors("sendbuf", [sendbuf], dt, M, dev)
     _check_tensors("recvbufs", recvbufs, dt, M, dev)
-    check_status(lib().vc_broadcast(ctypes.c_void_p(sendbuf.data_ptr()), _ptrs(recvbufs), n, M,
-                                    DTYPES[dt], _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(lib().vc_broadcast(ctypes.c_void_p(sendbuf.data_ptr()), _ptrs(recvbufs), n, M,
+                                        DTYPES[dt], _stream(stream, dev)))
 
 
 # ------------------------------------------------------ prepared calls --
@@ -275,7 +302,8 @@ class Prepared:
         self._device = device
 
     def __call__(self, stream=None):
-        check_status(self._fn(*self._args, _stream(stream, self._device)))
+        with _OnDevice(self._device):
+            check_status(self._fn(*self._args, _stream(stream, self._device)))
 
 
 def prepare_all_reduce(sendbufs, recvbufs=None, op: str = "sum", order: str = "ring"):
@@ -380,8 +408,9 @@ def vc_all_reduce_decomposed_noalloc(sendbufs, recvbufs=None, op: str = "sum",
     fn.argtypes = [vpp, vpp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                    ctypes.c_int, ctypes.c_void_p]
     fn.restype = ctypes.c_int
-    check_status(fn(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order],
-                    _stream(stream, dev)))
+    with _OnDevice(dev):
+        check_status(fn(_ptrs(sendbufs), _ptrs(recvbufs), n, M, DTYPES[dt], OPS[op], ORDERS[order],
+                        _stream(stream, dev)))
 
 
 # ------------------------------------------------------------ fused buckets --
@@ -474,27 +503,30 @@ class BucketPlan:
         """shards[r]: rank r's output, shard_count elements of the bucket's
         dtype on its device; disjoint from each other and from the tensors."""
         self._check_shards(shards)
-        check_status(lib().vc_reduce_scatter_bucket(
-            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
-            ctypes.c_void_p(self.in_ptrs.data_ptr()), _ptrs(shards), self.nranks,
-            self.bucket_count, DTYPES[self.dtype], OPS[op], _stream(stream, self.device)))
+        with _OnDevice(self.device):
+            check_status(lib().vc_reduce_scatter_bucket(
+                ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
+                ctypes.c_void_p(self.in_ptrs.data_ptr()), _ptrs(shards), self.nranks,
+                self.bucket_count, DTYPES[self.dtype], OPS[op], _stream(stream, self.device)))
 
     def all_gather(self, shards, stream=None):
         """shards[r] (shard_count elements) gathered back into every rank's
         output tensors: out[r][k] receives the bucket's elements of tensor k
         from the shards that hold them."""
         self._check_shards(shards)
-        check_status(lib().vc_all_gather_bucket(
-            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles, _ptrs(shards),
-            ctypes.c_void_p(self.out_ptrs.data_ptr()), self.nranks, self.bucket_count,
-            DTYPES[self.dtype], _stream(stream, self.device)))
+        with _OnDevice(self.device):
+            check_status(lib().vc_all_gather_bucket(
+                ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles, _ptrs(shards),
+                ctypes.c_void_p(self.out_ptrs.data_ptr()), self.nranks, self.bucket_count,
+                DTYPES[self.dtype], _stream(stream, self.device)))
 
     def all_reduce(self, op: str = "sum", stream=None):
-        check_status(lib().vc_all_reduce_bucket(
-            ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
-            ctypes.c_void_p(self.in_ptrs.data_ptr()), ctypes.c_void_p(self.out_ptrs.data_ptr()),
-            self.nranks, self.bucket_count, DTYPES[self.dtype], OPS[op],
-            _stream(stream, self.device)))
+        with _OnDevice(self.device):
+            check_status(lib().vc_all_reduce_bucket(
+                ctypes.c_void_p(self.tiles.data_ptr()), self.ntiles,
+                ctypes.c_void_p(self.in_ptrs.data_ptr()), ctypes.c_void_p(self.out_ptrs.data_ptr()),
+                self.nranks, self.bucket_count, DTYPES[self.dtype], OPS[op],
+                _stream(stream, self.device)))
 
 
 def _overlaps(a, b) -> bool:

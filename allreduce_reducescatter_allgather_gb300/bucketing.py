@@ -218,11 +218,13 @@ class GradientBuckets:
         L = _binding.lib()
         s = ctypes.c_void_p(stream.cuda_stream)
         for b, c in zip(self.buckets, self._calls(op, order)):
-            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
-                                                  b.ntiles, s))
+            with _binding._OnDevice(self.device):
+                _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
+                                                      b.ntiles, s))
             c(stream=stream)
-            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.unpack_tiles.data_ptr()),
-                                                  b.ntiles, s))
+            with _binding._OnDevice(self.device):
+                _binding.check_status(L.vc_copy_tiles(
+                    ctypes.c_void_p(b.unpack_tiles.data_ptr()), b.ntiles, s))
 
     def all_gather_tensors(self, stream=None):
         """FSDP's unpack: every bucket's shards (shards(bucket), e.g. after
@@ -255,6 +257,7 @@ class GradientBuckets:
         L = _binding.lib()
         s = ctypes.c_void_p(stream.cuda_stream)
         for b in self.buckets:
-            _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
-                                                  b.ntiles, s))
+            with _binding._OnDevice(self.device):
+                _binding.check_status(L.vc_copy_tiles(ctypes.c_void_p(b.pack_tiles.data_ptr()),
+                                                      b.ntiles, s))
         return self.reduce_scatter(op=op, order=order, stream=stream)
