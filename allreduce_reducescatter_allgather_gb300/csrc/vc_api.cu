@@ -226,29 +226,35 @@ int grid_blocks(long long units) {
     return (int)(b < 1 ? 1 : b);
 }
 
-cudaError_t launch_gather(const GatherParams& p_in, int esize, cudaStream_t st) {
+template <int ES>
+cudaError_t launch_gather_es(const GatherParams& p_in, cudaStream_t st) {
     GatherParams p = p_in;
-    const long long nvec = (p.M * esize + 15) / 16;
-    const int blocks = grid_blocks((nvec + kGatherSlots - 1) / kGatherSlots);
+    const long long nvec = (p.M * ES + 15) / 16;
+    const int slots = nvec >= kGatherWideVectors ? 8 : 2;
+    const int blocks = grid_blocks((nvec + slots - 1) / slots);
     if (blocks < 1) return cudaErrorInvalidConfiguration;
-    // Rank groups: double them while the grid is short of ~8 blocks per SM
+    // Rank groups: double them while the grid is short of 2 blocks per SM
     // and every group keeps at least 4 outputs (so the extra source reads stay
-    // a quarter of the writes at most).
-    const int target = 8 * sm_count();  // 8 blocks per SM
+    // a quarter of the writes at most).  (A target of 8 blocks per SM split
+    // 32 MiB x 8 ranks into two groups and cost 15 %.)
+    const int target = 2 * sm_count();
     int groups = 1;
     while ((long long)blocks * groups < target && p.n / (groups * 2) >= 4) groups *= 2;
     p.rpg = (p.n + groups - 1) / groups;
     // programmatic dependent launch: the gather may be scheduled while the
     // preceding kernel drains; it waits on griddepcontrol before any access
     const dim3 grid(blocks, groups);
-    cudaError_t e;
+    if (slots == 8) return launch_pdl(vc_ag_kernel<ES, 8>, grid, dim3(kThreads), st, p);
+    return launch_pdl(vc_ag_kernel<ES, 2>, grid, dim3(kThreads), st, p);
+}
+
+cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st) {
     switch (esize) {
-    case 2: e = launch_pdl(vc_ag_kernel<2>, grid, dim3(kThreads), st, p); break;
-    case 4: e = launch_pdl(vc_ag_kernel<4>, grid, dim3(kThreads), st, p); break;
-    case 8: e = launch_pdl(vc_ag_kernel<8>, grid, dim3(kThreads), st, p); break;
+    case 2: return launch_gather_es<2>(p, st);
+    case 4: return launch_gather_es<4>(p, st);
+    case 8: return launch_gather_es<8>(p, st);
     default: return cudaErrorInvalidValue;
     }
-    return e;
 }
 
 }  // namespace vc

@@ -925,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NT>()) vc_ar_kernel(const
 
 // AllGather: output index i comes from shard s = floor(i/q) at offset i - sq,
 // and is written to all N outputs.  It moves bits only, so it is typed by
-// element size alone.  Like the reductions, a thread takes kGatherSlots
+// element size alone.  Like the reductions, a thread takes S
 // vectors (blockDim.x apart) and loads all of them before it stores any.
 // When the M output indices alone give too few blocks for the GPU (small M,
 // many ranks), the outputs are split into groups along the grid's y axis:
@@ -935,7 +935,12 @@ template <> struct Bits<2> { using U = unsigned short; };
 template <> struct Bits<4> { using U = unsigned; };
 template <> struct Bits<8> { using U = unsigned long long; };
 
-constexpr int kGatherSlots = 8;
+// Vectors per thread: 8 when each rank holds at least kGatherWideVectors
+// 16-byte vectors, 2 below.  Measured on GB300 (fp32): 2 gain 10-15 % from 2
+// to 64 MiB per rank (more, smaller blocks balance the last wave); 8 stay
+// 1-4 % ahead from 256 MiB up; at 128 MiB the two are within a few percent
+// either way.
+constexpr long long kGatherWideVectors = 8LL << 20;  // 128 MiB of fp32
 
 template <int ES>
 __device__ __forceinline__ uint4 gather_load(const GatherParams& p, int s, long long i0) {
@@ -963,11 +968,10 @@ __device__ __noinline__ void gather_slot(const GatherParams& p, long long v, int
     }
 }
 
-template <int ES>
+template <int ES, int S>
 __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__ GatherParams p) {
     using U = typename Bits<ES>::U;
     constexpr int V = 16 / ES;
-    constexpr int S = kGatherSlots;
     // Launched with programmatic stream serialization, this grid may begin
     // while the kernel before it (the ReduceScatter of a decomposed
     // AllReduce) finishes; wait for that grid to complete and its writes to
