@@ -230,14 +230,17 @@ template <int ES>
 cudaError_t launch_gather_es(const GatherParams& p_in, cudaStream_t st) {
     GatherParams p = p_in;
     const long long nvec = (p.M * ES + 15) / 16;
-    const int slots = nvec >= kGatherWideVectors ? 8 : 2;
+    const int slots = nvec * p.n >= kGatherWideVectors ? 8 : 2;
     const int blocks = grid_blocks((nvec + slots - 1) / slots);
     if (blocks < 1) return cudaErrorInvalidConfiguration;
-    // Rank groups: double them while the grid is short of 2 blocks per SM
-    // and every group keeps at least 4 outputs (so the extra source reads stay
-    // a quarter of the writes at most).  (A target of 8 blocks per SM split
-    // 32 MiB x 8 ranks into two groups and cost 15 %.)
-    const int target = 2 * sm_count();
+    // Rank groups: double them while the grid is short of the target (8
+    // blocks per SM for the wide blocks of 8 vectors a thread, 2 for blocks
+    // of 2) and every group keeps at least 4 outputs (so the extra source
+    // reads stay a quarter of the writes at most).  Measured: with 2 vectors
+    // a target of 8 split 32 MiB x 8 ranks into two groups and cost 15 %;
+    // with 8 vectors a target of 2 left 32 MiB x 64 ranks one group of 1024
+    // blocks and cost 20 %.
+    const int target = (slots == 8 ? 8 : 2) * sm_count();
     int groups = 1;
     while ((long long)blocks * groups < target && p.n / (groups * 2) >= 4) groups *= 2;
     p.rpg = (p.n + groups - 1) / groups;

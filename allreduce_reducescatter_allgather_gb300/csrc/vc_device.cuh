@@ -935,12 +935,12 @@ template <> struct Bits<2> { using U = unsigned short; };
 template <> struct Bits<4> { using U = unsigned; };
 template <> struct Bits<8> { using U = unsigned long long; };
 
-// Vectors per thread: 8 when each rank holds at least kGatherWideVectors
-// 16-byte vectors, 2 below.  Measured on GB300 (fp32): 2 gain 10-15 % from 2
-// to 64 MiB per rank (more, smaller blocks balance the last wave); 8 stay
-// 1-4 % ahead from 256 MiB up; at 128 MiB the two are within a few percent
-// either way.
-constexpr long long kGatherWideVectors = 8LL << 20;  // 128 MiB of fp32
+// Vectors per thread: 8 when the call writes at least kGatherWideVectors
+// 16-byte vectors in all (N outputs), 2 below.  Measured on GB300 (fp32):
+// 2 gain 10-15 % at 2-64 MiB per rank (more, smaller blocks balance the last
+// wave); 8 stay 1-4 % ahead once the outputs reach ~1 GiB (256 MiB x 4
+// ranks, 32 MiB x 64 ranks).
+constexpr long long kGatherWideVectors = 64LL << 20;  // 1 GiB of output
 
 template <int ES>
 __device__ __forceinline__ uint4 gather_load(const GatherParams& p, int s, long long i0) {
