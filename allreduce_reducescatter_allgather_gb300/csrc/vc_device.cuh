@@ -983,7 +983,14 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
     const long long span = (long long)blockDim.x * S;
     const int r0 = (int)blockIdx.y * p.rpg;
     const int r1 = min(p.n, r0 + p.rpg);
-    for (long long b0 = (long long)blockIdx.x * span; b0 < nvec; b0 += (long long)gridDim.x * span) {
+    // The spans are taken from the end of the index space: blocks start in
+    // index order, so the first to run read the last shards, which a
+    // ReduceScatter just before (the decomposed AllReduce) wrote last and
+    // which are still in L2.  Taken from the start, they would be evicted by
+    // this kernel's own writes before it reached them.
+    const long long nspans = (nvec + span - 1) / span;
+    for (long long j = blockIdx.x; j < nspans; j += gridDim.x) {
+        const long long b0 = (nspans - 1 - j) * span;
         const long long v0 = b0 + threadIdx.x;
         const long long vlast = v0 + (long long)(S - 1) * blockDim.x;
         bool wide = false;
