@@ -247,8 +247,21 @@ cudaError_t launch_gather_es(const GatherParams& p_in, cudaStream_t st) {
     // programmatic dependent launch: the gather may be scheduled while the
     // preceding kernel drains; it waits on griddepcontrol before any access
     const dim3 grid(blocks, groups);
-    if (slots == 8) return launch_pdl(vc_ag_kernel<ES, 8>, grid, dim3(kThreads), st, p);
-    return launch_pdl(vc_ag_kernel<ES, 2>, grid, dim3(kThreads), st, p);
+    // 2-byte shards off the 16-byte grid (shard s's vectors start s*q
+    // elements into the index space, plus its base's own offset) take the
+    // instances that realign their loads across the warp.
+    if constexpr (ES == 2) {
+        const long long shards = (p.M + p.q - 1) / p.q;
+        bool realign = shards > 1 && (p.q * ES) % 16 != 0;
+        for (long long s = 0; s < shards && !realign; ++s)
+            realign = (reinterpret_cast<uintptr_t>(p.in[s]) & 15) != 0;
+        if (realign) {
+            if (slots == 8) return launch_pdl(vc_ag_kernel<ES, 8, true>, grid, dim3(kThreads), st, p);
+            return launch_pdl(vc_ag_kernel<ES, 2, true>, grid, dim3(kThreads), st, p);
+        }
+    }
+    if (slots == 8) return launch_pdl(vc_ag_kernel<ES, 8, false>, grid, dim3(kThreads), st, p);
+    return launch_pdl(vc_ag_kernel<ES, 2, false>, grid, dim3(kThreads), st, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, int esize, cudaStream_t st) {

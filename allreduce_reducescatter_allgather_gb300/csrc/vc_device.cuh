@@ -208,6 +208,153 @@ __device__ __forceinline__ uint4 ld_aligned(const void* p) {
     return v;
 }
 
+// ------------------------------------------------ warp-realigned access --
+//
+// A ReduceScatter writes, and an AllGather reads, a shard at offset i - cq of
+// the index i; when q elements are not a whole number of 16-byte vectors,
+// that offset is off the 16-byte grid by d bytes (the same d for the whole
+// shard).  A warp whose 32 lanes hold 32 consecutive vectors of one shard
+// (512 contiguous bytes) then realigns them among its lanes: lane t accesses
+// the aligned 16-byte block that starts d bytes before its own vector, and
+// takes the other part from its neighbour by shuffle.  Only the first lane
+// (the part of its block that lies inside the warp's bytes) and the last (the
+// d bytes past its block) access single elements; every byte accessed lies
+// inside the warp's 512 bytes.  All 32 lanes must call these together.
+//
+// Used for 2-byte elements only, where an off-grid vector otherwise takes
+// eight 2-byte accesses.  Measured on GB300 (64 MiB per rank, shards off the
+// grid): bf16 ReduceScatter at 3 ranks 0.68x -> 0.83x of the copy rate,
+// AllGather 0.91x -> 0.94x.  With 4- and 8-byte elements (at most four
+// accesses per vector) and in the streaming folds (N > 8 or run-time N), the
+// extra instructions cost as much as they save or more, so those keep the
+// element-aligned accesses.
+
+constexpr unsigned kFullWarp = 0xffffffffu;
+
+// Bytes [4*A0 + sh/8, ... + 16) of the 32-byte sequence w[0..7].
+template <int A0>
+__device__ __forceinline__ uint4 window_at(const unsigned (&w)[8], unsigned sh) {
+    return make_uint4(__funnelshift_r(w[A0], w[A0 + 1], sh), __funnelshift_r(w[A0 + 1], w[A0 + 2], sh),
+                      __funnelshift_r(w[A0 + 2], w[A0 + 3], sh),
+                      __funnelshift_r(w[A0 + 3], w[A0 + 4], sh));
+}
+
+// Bytes [off, off + 16) of the 32 bytes lo ++ hi, 0 < off < 16.
+__device__ __forceinline__ uint4 byte_window(const uint4& lo, const uint4& hi, int off) {
+    const unsigned w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const unsigned sh = (unsigned)(off & 3) * 8u;
+    switch (off >> 2) {
+    case 0: return window_at<0>(w, sh);
+    case 1: return window_at<1>(w, sh);
+    case 2: return window_at<2>(w, sh);
+    default: return window_at<3>(w, sh);
+    }
+}
+
+__device__ __forceinline__ uint4 shfl_up1(const uint4& v) {
+    return make_uint4(__shfl_up_sync(kFullWarp, v.x, 1), __shfl_up_sync(kFullWarp, v.y, 1),
+                      __shfl_up_sync(kFullWarp, v.z, 1), __shfl_up_sync(kFullWarp, v.w, 1));
+}
+
+__device__ __forceinline__ uint4 shfl_down1(const uint4& v) {
+    return make_uint4(__shfl_down_sync(kFullWarp, v.x, 1), __shfl_down_sync(kFullWarp, v.y, 1),
+                      __shfl_down_sync(kFullWarp, v.z, 1), __shfl_down_sync(kFullWarp, v.w, 1));
+}
+
+// Element k (of 16/ES) of v.  Called from fully unrolled loops, so k is a
+// constant after unrolling and the word index folds away.
+template <int ES>
+__device__ __forceinline__ unsigned long long elem_get(const uint4& v, int k) {
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (ES == 2) return (w[k / 2] >> (16 * (k % 2))) & 0xffffu;
+    else if constexpr (ES == 4) return w[k];
+    else return ((unsigned long long)w[2 * k + 1] << 32) | w[2 * k];
+}
+
+// Stores bytes [from, from + len) of v at p (the destination of byte
+// `from`), one element at a time; from and len are multiples of ES.
+template <int ES>
+__device__ __forceinline__ void st_bytes(unsigned char* p, const uint4& v, int from, int len) {
+#pragma unroll
+    for (int k = 0; k < 16 / ES; ++k) {
+        const int b = k * ES;
+        if (b >= from && b < from + len) {
+            unsigned char* e = p + (b - from);
+            if constexpr (ES == 2) {
+                *reinterpret_cast<unsigned short*>(e) = (unsigned short)elem_get<ES>(v, k);
+            } else if constexpr (ES == 4) {
+                *reinterpret_cast<unsigned*>(e) = (unsigned)elem_get<ES>(v, k);
+            } else {
+                *reinterpret_cast<unsigned long long*>(e) = elem_get<ES>(v, k);
+            }
+        }
+    }
+}
+
+// Loads bytes [from, to) of the aligned 16-byte block at blk into the same
+// byte positions of the result (the other bytes are zero), one element at a
+// time; from and to are multiples of ES.
+template <int ES>
+__device__ __forceinline__ uint4 ld_block_part(const unsigned char* blk, int from, int to) {
+    unsigned w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 16 / ES; ++k) {
+        const int b = k * ES;
+        if (b >= from && b < to) {
+            if constexpr (ES == 2) {
+                w[k / 2] |= (unsigned)*reinterpret_cast<const unsigned short*>(blk + b) << (16 * (k % 2));
+            } else if constexpr (ES == 4) {
+                w[k] = *reinterpret_cast<const unsigned*>(blk + b);
+            } else {
+                const unsigned long long e = *reinterpret_cast<const unsigned long long*>(blk + b);
+                w[2 * k] = (unsigned)e;
+                w[2 * k + 1] = (unsigned)(e >> 32);
+            }
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Lane t stores v, the t-th of the warp's 32 consecutive vectors, at dst.
+template <int ES>
+__device__ __forceinline__ void st_warp_realigned(void* dst, const uint4& v) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    const int d = (int)(a & 15);
+    if (d == 0) {
+        st16(dst, v);
+        return;
+    }
+    const int lane = (int)(threadIdx.x & 31);
+    const uint4 prev = shfl_up1(v);
+    unsigned char* blk = reinterpret_cast<unsigned char*>(a - (uintptr_t)d);
+    // the aligned block holding this vector's first 16 - d bytes: its first
+    // d bytes are the previous lane's last d (lane 0 stores only its own
+    // first 16 - d bytes)
+    if (lane > 0)
+        st16(blk, byte_window(prev, v, 16 - d));
+    else
+        st_bytes<ES>(static_cast<unsigned char*>(dst), v, 0, 16 - d);
+    // the last lane's final d bytes open the next block
+    if (lane == 31) st_bytes<ES>(blk + 16, v, 16 - d, d);
+}
+
+// Lane t loads the t-th of the warp's 32 consecutive vectors, at src.
+template <int ES>
+__device__ __forceinline__ uint4 ld_warp_realigned(const void* src) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    const int d = (int)(a & 15);
+    if (d == 0) return ld16(src);
+    const int lane = (int)(threadIdx.x & 31);
+    const unsigned char* blk = reinterpret_cast<const unsigned char*>(a - (uintptr_t)d);
+    // this lane's aligned block (lane 0: only its bytes d..15, the others
+    // lie before the warp's range); the vector is its bytes d..15 followed by
+    // the first d bytes of the next block
+    const uint4 cur = lane > 0 ? ld16(blk) : ld_block_part<ES>(blk, d, 16);
+    uint4 next = shfl_down1(cur);
+    if (lane == 31) next = ld_block_part<ES>(blk + 16, 0, d);
+    return byte_window(cur, next, d);
+}
+
 // ------------------------------------------------------------------- ops --
 
 // a (+) b with the running value on the left.  Floats: one IEEE single
@@ -717,17 +864,22 @@ __device__ __forceinline__ int chunk_of(long long i, long long q, float inv_q, i
 // --------------------------------------------------------------- kernels --
 
 // The result vector of elements i0 .. i0+V-1 (chunk c) to its destination:
-// AllReduce, all N outputs; ReduceScatter, the shard that owns it.
+// AllReduce, all N outputs; ReduceScatter, the shard that owns it (realigned
+// across the warp when `warp_shard`: the whole warp stores 32 consecutive
+// vectors of that shard together).
 template <class T, int NT, bool RS, class A, int V>
 __device__ __forceinline__ void store_result(const ReduceParams& p, int c, long long i0,
-                                             Vec<A, V>& acc) {
+                                             Vec<A, V>& acc, bool warp_shard) {
     if (p.avg) {
 #pragma unroll
         for (int k = 0; k < V; ++k) acc.x[k] = avg_div(acc.x[k], p.n);
     }
     if constexpr (RS) {
         T* dst = static_cast<T*>(p.out[c]) + (i0 - (long long)c * p.q);
-        st_aligned<sizeof(T)>(dst, pack(acc, (T*)nullptr));
+        if (warp_shard)
+            st_warp_realigned<sizeof(T)>(dst, pack(acc, (T*)nullptr));
+        else
+            st_aligned<sizeof(T)>(dst, pack(acc, (T*)nullptr));
     } else {
         const uint4 u = pack(acc, (T*)nullptr);
         if constexpr (NT > 0) {
@@ -770,7 +922,7 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
         VecLoader<T> ld{p, i0};
         const int sel = (ORDER == kOrderDoubleTree) ? (i0 >= p.half) : c;
         auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
-        store_result<T, NT, RS>(p, c, i0, acc);
+        store_result<T, NT, RS>(p, c, i0, acc, false);
     } else {
         for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
     }
@@ -835,6 +987,18 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
         }
         // the fold's selector: the ring's chunk, or the double tree's half
         const int sel = (ORDER == kOrderDoubleTree) ? (int)(v0 * V >= p.half) : c;
+        // ReduceScatter of 2-byte elements with the operands preloaded: when
+        // every lane of the warp takes the vector path into the same shard,
+        // the warp's vectors of each slot are 512 contiguous bytes of that
+        // shard, stored realigned (every lane of the
+        // block reaches this point: the loop bounds are the same for all; the
+        // shuffle runs in every lane, before the test: a lane that skipped it
+        // would leave the others waiting in it)
+        bool warp_shard = false;
+        if constexpr (RS && kPre && sizeof(T) == 2) {
+            const int c_lane0 = __shfl_sync(kFullWarp, c, 0);
+            warp_shard = __all_sync(kFullWarp, wide && c == c_lane0);
+        }
         if (wide) {
             if constexpr (kPre) {
                 uint4 buf[NT][U];
@@ -848,7 +1012,8 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
                 for (int u = 0; u < U; ++u) {
                     PreLoader<T, NT, U> ld{buf, u};
                     auto acc = fold<Op, ORDER, NT>(ld, NT, sel);
-                    store_result<T, NT, RS>(p, c, (v0 + (long long)u * blockDim.x) * V, acc);
+                    store_result<T, NT, RS>(p, c, (v0 + (long long)u * blockDim.x) * V, acc,
+                                            warp_shard);
                 }
             } else if constexpr (kTable) {
                 static_assert(U == 1, "streaming folds take one vector per thread");
@@ -874,12 +1039,12 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
                 static_assert(U == 1, "streaming folds take one vector per thread");
                 SharedTableLoader<T> ld{s_in, v0 * V};
                 auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
-                store_result<T, NT, RS>(p, c, v0 * V, acc);
+                store_result<T, NT, RS>(p, c, v0 * V, acc, false);
             } else {
                 static_assert(U == 1, "streaming folds take one vector per thread");
                 VecLoader<T> ld{p, v0 * V};
                 auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
-                store_result<T, NT, RS>(p, c, v0 * V, acc);
+                store_result<T, NT, RS>(p, c, v0 * V, acc, false);
             }
         } else {
 #pragma unroll 1
@@ -968,7 +1133,11 @@ __device__ __noinline__ void gather_slot(const GatherParams& p, long long v, int
     }
 }
 
-template <int ES, int S>
+// REALIGN (2-byte elements only): some shard that the call reads sits off the
+// 16-byte grid (q elements not a whole number of vectors, or a shard base off
+// the grid); the host picks the instance, so every other call runs code
+// without the warp-realigned loads.
+template <int ES, int S, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__ GatherParams p) {
     using U = typename Bits<ES>::U;
     constexpr int V = 16 / ES;
@@ -1000,10 +1169,28 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
             const long long end = vlast * V + V;
             wide = end <= p.M && end <= (long long)(s + 1) * p.q;
         }
+        // when every lane of the warp takes the vector path from the same
+        // shard, the warp's vectors of each slot are 512 contiguous bytes of
+        // it, loaded realigned (the loop bounds are the same for all lanes;
+        // the shuffle runs in every lane, before the test: a lane that
+        // skipped it would leave the others waiting in it)
+        bool warp_shard = false;
+        if constexpr (REALIGN) {
+            const int s_lane0 = __shfl_sync(kFullWarp, s, 0);
+            warp_shard = __all_sync(kFullWarp, wide && s == s_lane0);
+        }
         if (wide) {
             uint4 val[S];
+            if (warp_shard) {
+                const U* src = static_cast<const U*>(p.in[s]) + (v0 * V - (long long)s * p.q);
 #pragma unroll
-            for (int u = 0; u < S; ++u) val[u] = gather_load<ES>(p, s, (v0 + (long long)u * blockDim.x) * V);
+                for (int u = 0; u < S; ++u)
+                    val[u] = ld_warp_realigned<ES>(src + (long long)u * blockDim.x * V);
+            } else {
+#pragma unroll
+                for (int u = 0; u < S; ++u)
+                    val[u] = gather_load<ES>(p, s, (v0 + (long long)u * blockDim.x) * V);
+            }
             for (int r = r0; r < r1; ++r) {
                 U* dst = static_cast<U*>(p.out[r]) + v0 * V;
 #pragma unroll

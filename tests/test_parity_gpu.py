@@ -5,8 +5,9 @@ a float result in a different order must lie within the bound the tests name.
 Small and medium cases compare every element of every output; the full-size
 four-rank 256 MiB workload compares a million sampled indices (plus every
 chunk boundary) one by one, and checks properties that hold at any size on
-the device.  Output buffers carry guard elements after their end that must
-come back untouched.
+the device.  Output buffers carry guard elements after their end (and, when
+they start inside their allocation, before it) that must come back
+untouched.
 """
 from __future__ import annotations
 
@@ -71,6 +72,8 @@ class Guarded:
         for big in self.bigs:
             tail = big[self.offset + self.numel:]
             assert env.torch.all(tail == sentinel(self.dtype)).item(), "guard overwritten"
+            head = big[:self.offset]
+            assert env.torch.all(head == sentinel(self.dtype)).item(), "head guard overwritten"
 
     def host(self):
         return [to_host(v, self.dtype) for v in self.views]
@@ -537,6 +540,50 @@ def test_in_place(env, dtype):
         for r in range(n):
             assert_bits_equal(to_host(d[r], dtype), oy[r], dtype, f"in-place AR {order}")
             assert_bits_equal(to_host(d2[r], dtype), oy[r], dtype, f"in-place dec {order}")
+
+
+ESIZE = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}
+
+
+@pytest.mark.parametrize("dtype", SWEEP_DTYPES)
+def test_shards_off_the_vector_grid(env, dtype):
+    """When q elements are not a whole number of 16-byte vectors, shard c
+    holds the indices from cq on, so its vectors sit off the 16-byte grid by
+    a different amount for each c; a shard buffer may also start off the
+    grid itself.  ReduceScatter stores and AllGather loads then realign
+    across the warp.  Every offset a shard can take (q = 1 and q = -1 modulo
+    the vector width, eight ranks, shard bases moved by 0 .. V-1 elements,
+    inputs and outputs aligned), several warps per shard, a padded last
+    shard; guards before and after every shard and output."""
+    vc, torch = env.vc, env.torch
+    V = 16 // ESIZE[dtype]
+    n = 8
+    k = 0
+    for q in (V * 301 + 1, V * 97 + V - 1):
+        M = n * q - 3
+        for shift in range(V):
+            op = SWEEP_OPS[k % len(SWEEP_OPS)]
+            order = ORDERS[k % len(ORDERS)] if dtype in ("float32", "bfloat16") else "ring"
+            k += 1
+            xs = gen(dtype, n, M, seed=7100 + 13 * q + shift)
+            if op == "prod" and dtype in ("float32", "bfloat16"):
+                xs = gen_prod_floats(dtype, n, M)
+            d = to_device(torch, xs, dtype, env.dev)
+            z = Guarded(env, n, q, dtype, shift)
+            g = Guarded(env, n, M, dtype)
+            vc.vc_reduce_scatter(d, z.views, op=op, order=order)
+            vc.vc_all_gather(z.views, g.views)
+            torch.cuda.synchronize()
+            z.check_guards(env)
+            g.check_guards(env)
+            oz = oracle.reduce_scatter(xs, dtype, op, order)
+            zh = z.host()
+            og = oracle.all_gather(zh, M, dtype)
+            gh = g.host()
+            for r in range(n):
+                t = f"{dtype} {op} {order} q={q} shift={shift} rank {r}"
+                assert_bits_equal(zh[r], oz[r], dtype, "RS " + t)
+                assert_bits_equal(gh[r], og[r], dtype, "AG " + t)
 
 
 def test_all_gather_from_arbitrary_shards(env):
