@@ -553,13 +553,14 @@ def test_shards_off_the_vector_grid(env, dtype):
     grid itself.  ReduceScatter stores and AllGather loads then realign
     across the warp.  Every offset a shard can take (q = 1 and q = -1 modulo
     the vector width, eight ranks, shard bases moved by 0 .. V-1 elements,
-    inputs and outputs aligned), several warps per shard, a padded last
-    shard; guards before and after every shard and output."""
+    inputs and outputs aligned), and q a whole number of vectors with only
+    the bases moved; several warps per shard, a padded last shard; guards
+    before and after every shard and output."""
     vc, torch = env.vc, env.torch
     V = 16 // ESIZE[dtype]
     n = 8
     k = 0
-    for q in (V * 301 + 1, V * 97 + V - 1):
+    for q in (V * 301 + 1, V * 97 + V - 1, V * 160):
         M = n * q - 3
         for shift in range(V):
             op = SWEEP_OPS[k % len(SWEEP_OPS)]
