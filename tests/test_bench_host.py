@@ -1,5 +1,6 @@
-"""Host-side logic of bench.py on CPU: the byte accounting of a step and the
-max-over-ranks / sum-over-ranks aggregation, the latter with two gloo ranks."""
+"""Host-side logic of bench.py on CPU: the byte accounting of a step, the
+recorded-traffic lookup and the L2 note, and the max-over-ranks /
+sum-over-ranks aggregation, the latter with two gloo ranks."""
 from __future__ import annotations
 
 import os
@@ -17,6 +18,36 @@ def test_step_bytes():
     assert b["all_gather"] == M * s + n * M * s
     assert b["fused_ar"] == 2 * n * M * s
     assert b["step"] == 4 * n * M * s + 2 * M * s
+
+
+def test_recorded_traffic_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu record only while the
+    measured kernels' code still hashes to the digest recorded with it."""
+    rec = bench.ROOT / "profiles" / "dram_traffic.txt"
+    text = rec.read_text()
+    got = bench.recorded_traffic("vc_ar_kernel", "n4_256mib_f32_normal")
+    if f"source_sha: {bench.source_digest()}" in text:
+        assert got is not None and got > 0
+    else:
+        assert got is None
+    # the same record with another digest is ignored
+    fake = tmp_path / "repo"
+    (fake / "profiles").mkdir(parents=True)
+    (fake / "profiles" / "dram_traffic.txt").write_text(
+        text.replace(f"source_sha: {bench.source_digest()}", "source_sha: 0000000000000000"))
+    monkeypatch.setattr(bench, "ROOT", fake)
+    monkeypatch.setattr(bench, "source_digest", lambda: "0000000000000000")
+    assert bench.recorded_traffic("vc_ar_kernel", "n4_256mib_f32_normal") > 0
+    assert bench.recorded_traffic("vc_ar_kernel", "another_workload") is None
+    monkeypatch.setattr(bench, "source_digest", lambda: "ffffffffffffffff")
+    assert bench.recorded_traffic("vc_ar_kernel", "n4_256mib_f32_normal") is None
+
+
+def test_l2_note_names_small_cases():
+    """A step whose inputs fit twice in the 129 MB L2 is called out as a
+    small case; the full-size workload is not."""
+    assert "far larger" in bench.l2_note(4 * 256 << 20)
+    assert "small case" in bench.l2_note(4 * 8 << 20)
 
 
 def _free_port():
