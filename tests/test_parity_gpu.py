@@ -11,7 +11,6 @@ untouched.
 """
 from __future__ import annotations
 
-import math
 from types import SimpleNamespace
 
 import numpy as np
@@ -20,7 +19,7 @@ import pytest
 import oracle
 import synthetic_inputs as si
 from conftest import ints, read_golden
-from gpu_util import assert_bits_equal, bits, to_device, to_host, torch_dtype
+from gpu_util import assert_bits_equal, to_device, to_host, torch_dtype
 
 pytestmark = pytest.mark.gpu
 

@@ -13,7 +13,6 @@ from __future__ import annotations
 
 import ctypes
 
-import numpy as np
 import pytest
 
 import synthetic_inputs as si
