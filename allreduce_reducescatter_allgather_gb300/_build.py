@@ -85,10 +85,10 @@ def build_library(force: bool = False, jobs: int | None = None) -> Path:
     jobs_list = [(Path(s).stem, s, []) for s in SOURCES]
     jobs_list += [(stem, INSTANCE_SOURCE, defs) for stem, defs in INSTANCES]
     jobs_list += [(stem, BUCKET_SOURCE, defs) for stem, defs in BUCKET_INSTANCES]
-    # the largest slices first (double tree, tree, ring and bucket), so the
-    # pool finishes together
-    jobs_list.sort(key=lambda j: -int(j[0][-1]) if j[1] == INSTANCE_SOURCE
-                   else (0 if j[1] == BUCKET_SOURCE else 1))
+    # the longest units first (the bucket slices, then the double tree, tree
+    # and ring slices, then the rest), so the pool finishes together
+    jobs_list.sort(key=lambda j: -3 if j[1] == BUCKET_SOURCE
+                   else (-int(j[0][-1]) if j[1] == INSTANCE_SOURCE else 1))
     jobs = jobs or max(1, os.cpu_count() or 4)
     with ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(compile_one, jobs_list))
