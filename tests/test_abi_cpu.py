@@ -230,6 +230,36 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         _binding.lib()
 
 
+def test_binding_refuses_host_tensors():
+    """Every entry point of the binding refuses tensors in host memory with
+    an error before anything runs: there is no CPU path to fall back on."""
+    torch = pytest.importorskip("torch")
+    import allreduce_reducescatter_allgather_gb300 as vc
+    n, M = 4, 10
+    q = -(-M // n)
+    xs = [torch.zeros(M) for _ in range(n)]
+    ys = [torch.zeros(M) for _ in range(n)]
+    zs = [torch.zeros(q) for _ in range(n)]
+    calls = [
+        lambda: vc.vc_all_reduce(xs, ys),
+        lambda: vc.vc_all_reduce(xs),
+        lambda: vc.vc_reduce_scatter(xs, zs),
+        lambda: vc.vc_all_gather(zs, ys),
+        lambda: vc.vc_all_reduce_decomposed(xs, zs, ys),
+        lambda: vc.vc_all_reduce_decomposed_noalloc(xs, ys),
+        lambda: vc.vc_reduce(xs, ys[0]),
+        lambda: vc.vc_broadcast(xs[0], ys),
+        lambda: vc.prepare_all_reduce(xs, ys),
+        lambda: vc.prepare_all_reduce_decomposed(xs, zs, ys),
+        lambda: vc.prepare_reduce_scatter(xs, zs),
+        lambda: vc.prepare_all_gather(zs, ys),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="not a CUDA tensor"):
+            call()
+    assert all(torch.count_nonzero(y) == 0 for y in ys)
+
+
 def test_element_misaligned_pointer_rejected(vc):
     """A buffer not aligned to its element size is rejected on the host (the
     element-wise kernel paths would otherwise access it misaligned)."""
