@@ -6,9 +6,11 @@
 // of the N rank buffers, folds the N vectors lane by lane in the order's fixed
 // tree, and stores the result (AllReduce: to all N outputs; ReduceScatter: to
 // the shard that owns the index).  No block waits on another: no flag, no
-// inter-block traffic.  (The one barrier is a block's own __syncthreads after
-// it copies the pointer table to shared memory; the one wait is the
-// AllGather's grid dependency on the kernel before it.)  The work is bound by
+// inter-block traffic.  (The barriers are a block's own __syncthreads after
+// it copies the pointer table to shared memory, and the warp-wide shuffles
+// of the realigned shard accesses; the one wait is each kernel's grid
+// dependency on the kernel before it, which the hardware releases when that
+// kernel completes.)  The work is bound by
 // HBM bandwidth, so the design is about keeping many 16-byte loads in flight
 // (up to 16 independent loads per thread, many more blocks than are
 // resident) and about never re-reading a byte.
