@@ -36,8 +36,7 @@
  *    data; for even N the second is the first with every rank number shifted
  *    by one, for odd N its mirror image.
  *
- * Readings where the pages are silent (each one is also listed in the design
- * notes):
+ * Readings where the pages are silent:
  *  - integer ops accumulate in 64 bits and wrap modulo 2^64 (int32 results
  *    are the low 32 bits);
  *  - AVG is the SUM in the chosen order followed by one division by N: an
