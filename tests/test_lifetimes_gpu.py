@@ -1,16 +1,25 @@
 """Buffer lifetimes of the decomposed AllReduce and the ZeRO-style RS-only
-flow ("NCCL 专家课程 07", 显存实验: RS-only keeps 64 of 256 MiB; the naive RS+AG
-lifetime peaks at 576 MiB, releasing the input first brings it to 320 MiB).
-Here the release is stream-ordered (no synchronize) and the results must be
-the fused AllReduce's bits."""
+flow ("NCCL 专家课程 07", 显存实验必须区分 steady 与 peak: RS-only keeps 64 of
+256 MiB; the naive RS+AG lifetime peaks at 576 MiB, releasing the input first
+brings it to 320 MiB; and ZeRO/FSDP 为什么停在 ReduceScatter).  Here the release
+is stream-ordered (no synchronize).  The shards and outputs of every flow are
+compared bit for bit with the CPU oracle on the same host inputs: the oracle's
+ReduceScatter for the kept shards, its AllReduce for the gathered outputs
+(same order, so the bits must agree)."""
 from __future__ import annotations
 
 import pytest
 
+import oracle
 import synthetic_inputs as si
+from gpu_util import assert_bits_equal, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 MiB = 1 << 20
+
+CASES = [("float32", "ring", "sum"), ("float32", "pairwise_tree", "sum"),
+         ("bfloat16", "recursive_halving", "avg"), ("int64", "ring", "prod"),
+         ("float32", "double_binary_tree", "max")]
 
 
 @pytest.fixture(scope="module")
@@ -27,22 +36,49 @@ def env():
     return torch, vc, lifetimes, dev
 
 
-@pytest.mark.parametrize("dtype,order", [("float32", "ring"), ("float32", "pairwise_tree"),
-                                         ("bfloat16", "recursive_halving"), ("int64", "ring")])
-def test_low_peak_decomposed_matches_fused(env, dtype, order):
+def _host_inputs(dtype, n, M, seed):
+    if dtype == "int64":
+        return si.generate(dtype, "uniform_int", n, M, seed=seed, lo=-100, hi=100)
+    return si.generate(dtype, "uniform_pm1", n, M, seed=seed)
+
+
+@pytest.mark.parametrize("dtype,order,op", CASES)
+def test_low_peak_decomposed_matches_oracle(env, dtype, order, op):
     torch, vc, lt, dev = env
     n, M = 8, 1_000_003
-    dist = "uniform_pm1" if dtype != "int64" else "uniform_int"
-    kw = {} if dtype != "int64" else {"lo": -100, "hi": 100}
-    base = si.generate_device(torch, dtype, dist, n, M, seed=3, device=dev, **kw)
-    ref = [torch.empty_like(t) for t in base]
-    vc.vc_all_reduce(base, ref, order=order)
-    inputs = [t.clone() for t in base]
-    outs = lt.all_reduce_decomposed_low_peak(inputs, order=order)
+    xs = _host_inputs(dtype, n, M, seed=3)
+    want = oracle.all_reduce(xs, dtype, op, order)
+    inputs = to_device(torch, xs, dtype, dev)
+    outs = lt.all_reduce_decomposed_low_peak(inputs, op=op, order=order)
     torch.cuda.synchronize()
     assert inputs == []  # ownership taken
     for r in range(n):
-        assert torch.equal(outs[r], ref[r])
+        assert_bits_equal(to_host(outs[r], dtype), want[r], dtype, f"low-peak AR rank {r}")
+
+
+@pytest.mark.parametrize("dtype,order,op", CASES)
+def test_reduce_scatter_keep_shards_matches_oracle(env, dtype, order, op):
+    """The ZeRO step: only the shards survive, and each is the oracle's
+    ReduceScatter shard (padding tail included)."""
+    torch, vc, lt, dev = env
+    n, M = 8, 1_000_003
+    xs = _host_inputs(dtype, n, M, seed=4)
+    want = oracle.reduce_scatter(xs, dtype, op, order)
+    inputs = to_device(torch, xs, dtype, dev)
+    shards = lt.reduce_scatter_keep_shards(inputs, op=op, order=order)
+    torch.cuda.synchronize()
+    assert inputs == []
+    q = vc.vc_shard_count(M, n)
+    assert len(shards) == n and all(s.numel() == q for s in shards)
+    for r in range(n):
+        assert_bits_equal(to_host(shards[r], dtype), want[r], dtype, f"kept shard {r}")
+    # the shards gathered into fresh outputs give the oracle's AllReduce
+    outs = lt.all_gather_new(shards, M)
+    torch.cuda.synchronize()
+    assert shards == []
+    want_ar = oracle.all_reduce(xs, dtype, op, order)
+    for r in range(n):
+        assert_bits_equal(to_host(outs[r], dtype), want_ar[r], dtype, f"gathered rank {r}")
 
 
 def _peak(torch, dev, fn):
@@ -95,13 +131,15 @@ def test_peak_and_steady_memory(env):
 def test_inputs_from_another_stream(env):
     """Inputs written on a side stream: the caller orders its stream after
     the producer; the helper records the inputs on the stream that reads
-    them, so their memory is not handed out before the ReduceScatter ran."""
+    them, so their memory is not handed out before the ReduceScatter ran.
+    The outputs are the oracle's AllReduce of the host inputs."""
     torch, vc, lt, dev = env
     n, M = 4, 1 << 22
-    src = si.generate_device(torch, "float32", "uniform_pm1", n, M, seed=2, device=dev)
-    ref = [torch.empty_like(t) for t in src]
-    vc.vc_all_reduce(src, ref)
+    xs = _host_inputs("float32", n, M, seed=2)
+    want = oracle.all_reduce(xs, "float32", "sum", "ring")
+    src = to_device(torch, xs, "float32", dev)
     side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
         inputs = [t * 1.0 for t in src]
     torch.cuda.current_stream(dev).wait_stream(side)
@@ -112,5 +150,5 @@ def test_inputs_from_another_stream(env):
         junk = [torch.full((M,), 7.0, device=dev) for _ in range(n)]
     torch.cuda.synchronize()
     for r in range(n):
-        assert torch.equal(outs[r], ref[r])
+        assert_bits_equal(to_host(outs[r], "float32"), want[r], "float32", f"rank {r}")
     del junk

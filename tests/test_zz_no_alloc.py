@@ -3,11 +3,13 @@ cannot allocate device memory (a framework allocator owns the memory, the path
 cannot pay for cudaMalloc, or the caller holds only its input and output
 buffers).  Its shards live in a fixed 32 MiB scratch array inside the library.
 
-Checked through the C ABI against the existing vc_all_reduce_decomposed (same
-order, so bit for bit) on two calls in a row with different inputs: the
-second call must not see anything the first left in the shared scratch.
-Kept in a file of its own that pytest collects last; it passes alone in a
-fresh process and after the other tests.
+Checked through the C ABI on two calls in a row with different inputs (the
+second call must not see anything the first left in the shared scratch):
+against the CPU oracle's decomposed AllReduce of the same host inputs, and
+against the existing vc_all_reduce_decomposed with caller-allocated shards.
+Both in the same order, so bit for bit.  Kept in a file of its own that
+pytest collects last; it passes alone in a fresh process and after the other
+tests.
 """
 from __future__ import annotations
 
@@ -15,6 +17,7 @@ import ctypes
 
 import pytest
 
+import oracle
 import synthetic_inputs as si
 from gpu_util import assert_bits_equal, to_device, to_host
 
@@ -51,7 +54,7 @@ def _inputs(dtype, n, M, seed):
 
 
 @pytest.mark.parametrize("dtype,n,M,op,order", CASES)
-def test_noalloc_matches_decomposed_on_two_calls(env, dtype, n, M, op, order):
+def test_noalloc_matches_oracle_and_decomposed_on_two_calls(env, dtype, n, M, op, order):
     torch, vc, dev = env
     from allreduce_reducescatter_allgather_gb300._binding import (
         DTYPES, OPS, ORDERS, lib, pointer_table)
@@ -77,9 +80,12 @@ def test_noalloc_matches_decomposed_on_two_calls(env, dtype, n, M, op, order):
                     ORDERS[order], ctypes.c_void_p(stream.cuda_stream))
         assert status == 0, L.vc_status_string(status)
         torch.cuda.synchronize()
+        _, want = oracle.all_reduce_decomposed(xs, dtype, op, order)
         for r in range(n):
+            assert_bits_equal(to_host(got[r], dtype), want[r], dtype,
+                              f"call {call} rank {r} vs oracle")
             assert_bits_equal(to_host(got[r], dtype), to_host(ref[r], dtype), dtype,
-                              f"call {call} rank {r}")
+                              f"call {call} rank {r} vs vc_all_reduce_decomposed")
 
 
 def test_noalloc_in_place_through_binding(env):
@@ -92,7 +98,9 @@ def test_noalloc_in_place_through_binding(env):
     vc.vc_all_reduce_decomposed(d, [torch.empty(q, device=dev) for _ in range(n)], ref)
     vc.vc_all_reduce_decomposed_noalloc(d)  # in place
     torch.cuda.synchronize()
+    _, want = oracle.all_reduce_decomposed(xs, "float32", "sum", "ring")
     for r in range(n):
+        assert_bits_equal(to_host(d[r], "float32"), want[r], "float32", f"rank {r} vs oracle")
         assert torch.equal(d[r], ref[r])
 
 
