@@ -51,9 +51,11 @@ __global__ void __launch_bounds__(kThreads) vc_bucket_gather_kernel(const __grid
         const int tn = t + gridDim.x;
         vc_bucket_tile_t next_tile = tile;
         if (tn < p.ntiles) next_tile = p.tiles[tn];
-        const int c = (int)(tile.bucket_offset / p.q);
-        const U* src = static_cast<const U*>(p.shard[c]) + (tile.bucket_offset - (long long)c * p.q);
-        const long long nvec = (tile.flags & 1) ? tile.count / V : 0;
+        // a tile planned for another bucket is skipped (tile_in_plan)
+        const bool valid = tile_in_plan(tile, p);
+        const int c = valid ? (int)(tile.bucket_offset / p.q) : 0;
+        const U* src = static_cast<const U*>(p.shard[c]) + (valid ? tile.bucket_offset - (long long)c * p.q : 0);
+        const long long nvec = (valid && (tile.flags & 1)) ? tile.count / V : 0;
         for (long long v0 = threadIdx.x; v0 < nvec; v0 += (long long)blockDim.x * S) {
             uint4 val[S];
 #pragma unroll
@@ -70,7 +72,8 @@ __global__ void __launch_bounds__(kThreads) vc_bucket_gather_kernel(const __grid
                 }
             }
         }
-        for (long long j = nvec * V + threadIdx.x; j < tile.count; j += blockDim.x) {
+        const long long tail_end = valid ? tile.count : 0;
+        for (long long j = nvec * V + threadIdx.x; j < tail_end; j += blockDim.x) {
             const U x = src[j];
             for (int r = 0; r < p.n; ++r) static_cast<U*>(s_out[r])[tile.tensor_offset + j] = x;
         }

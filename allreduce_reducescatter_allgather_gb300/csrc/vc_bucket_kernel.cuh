@@ -87,6 +87,18 @@ __device__ __forceinline__ void bucket_element(const BucketParams& p, const void
     }
 }
 
+// A tile as vc_bucket_plan makes it lies inside the bucket and inside one
+// ring chunk.  Tiles planned for another bucket_count (or N) may not: their
+// chunk index could name a shard or a ring rotation that does not exist.
+// The kernels skip such a tile (every thread of the block sees the same
+// tile, so the block stays uniform) instead of touching memory through it.
+__device__ __forceinline__ bool tile_in_plan(const vc_bucket_tile_t& t, const BucketParams& p) {
+    if (t.bucket_offset < 0 || t.count < 0 || t.bucket_offset + t.count > p.bucket_count)
+        return false;
+    const long long c = t.bucket_offset / p.q;
+    return c < p.n && t.bucket_offset + t.count <= (c + 1) * p.q;
+}
+
 // ReduceScatter: the shard positions no tensor covers, from bucket offset
 // lo to hi.  Below bucket_count they are the gaps between tensors, which
 // the packed bucket holds as zeros on every rank: every op reduces zeros
@@ -95,6 +107,8 @@ __device__ __forceinline__ void bucket_element(const BucketParams& p, const void
 template <class T, class Op>
 __device__ __forceinline__ void bucket_fill(const BucketParams& p, long long lo, long long hi) {
     using A = typename Traits<T>::Acc;
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > (long long)p.n * p.q ? (long long)p.n * p.q : hi;
     for (long long b = lo + threadIdx.x; b < hi; b += blockDim.x) {
         const int c = (int)(b / p.q);
         const A v = b < p.bucket_count ? A(0) : (p.avg ? A(0) : Identity<T, Op>::get());
@@ -142,8 +156,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         long long next_start = 0;  // ReduceScatter: where the next tile starts
         if constexpr (RS)
             next_start = t + 1 < p.ntiles ? p.tiles[t + 1].bucket_offset : (long long)p.n * p.q;
-        const int c = (int)(tile.bucket_offset / p.q);  // the tile's ring chunk
-        const long long nvec = (tile.flags & 1) ? tile.count / V : 0;
+        const bool valid = tile_in_plan(tile, p);  // the same in every thread
+        const int c = valid ? (int)(tile.bucket_offset / p.q) : 0;  // the tile's ring chunk
+        const long long nvec = (valid && (tile.flags & 1)) ? tile.count / V : 0;
         const long long span = (long long)blockDim.x * U;
         for (long long b0 = 0; b0 < nvec; b0 += span) {
             const long long v0 = b0 + threadIdx.x;
@@ -176,12 +191,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         // the tile's tail, or all of it when its addresses are not aligned
-        for (long long j = nvec * V + threadIdx.x; j < tile.count; j += blockDim.x)
+        const long long tail_end = valid ? tile.count : 0;
+        for (long long j = nvec * V + threadIdx.x; j < tail_end; j += blockDim.x)
             bucket_element<T, Op, RS>(p, s_in, s_out, c, tile.tensor_offset + j,
                                       tile.bucket_offset + j);
         if constexpr (RS) {
-            if (t == 0) bucket_fill<T, Op>(p, 0, tile.bucket_offset);
-            bucket_fill<T, Op>(p, tile.bucket_offset + tile.count, next_start);
+            if (valid) {
+                if (t == 0) bucket_fill<T, Op>(p, 0, tile.bucket_offset);
+                bucket_fill<T, Op>(p, tile.bucket_offset + tile.count, next_start);
+            }
         }
         if (tn < p.ntiles) {
             tile = next_tile;

@@ -2,11 +2,15 @@
 // cannot allocate device memory.
 //
 // The N intermediate shards, which vc_all_reduce_decomposed takes from the
-// caller, live here in one file-scope device array of a fixed size.  Every
-// GPU that loads this library holds that array until the process exits.  The
-// call itself allocates nothing: it looks up the array's device address once
-// per device, carves it into N shards and launches the same ReduceScatter and
-// AllGather kernels as the other entry points.
+// caller, live here in one file-scope device array of a fixed size.  This
+// file holds no kernel, so the array is the only content of its device-code
+// module: under lazy module loading it is placed on a device at the first
+// call there (the cudaGetSymbolAddress below), eagerly when the context is
+// set up otherwise, and held until the process exits.  The call itself
+// allocates nothing: it looks up the array's device address once per device,
+// carves it into N shards and launches the same ReduceScatter and AllGather
+// kernels as the other entry points.  The cached address does not survive a
+// cudaDeviceReset of its device.
 #include <cstdlib>
 #include <cstring>
 #include <mutex>

@@ -290,7 +290,12 @@ vc_status_t vc_bucket_plan(const void *const *sendbufs, void *const *recvbufs,
  * op: any vc_op_t (AVG divides by nranks).
  * The tables live in device memory, so the library checks only the scalar
  * arguments here; tables that differ from the planned ones are undefined
- * behaviour, as for any device copy.  ntiles == 0 launches nothing. */
+ * behaviour, as for any device copy.  One guard runs on the device, in all
+ * three bucket calls: a tile that does not lie inside [0, bucket_count) and
+ * inside one ring chunk of this bucket (tiles planned with another
+ * bucket_count or nranks) is skipped, so a mismatched bucket_count leaves
+ * those elements unwritten instead of reaching a shard that does not exist.
+ * ntiles == 0 launches nothing. */
 vc_status_t vc_all_reduce_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
                                  const void *const *dev_sendbufs, void *const *dev_recvbufs,
                                  int nranks, size_t bucket_count, vc_dtype_t dtype, vc_op_t op,
@@ -333,7 +338,9 @@ vc_status_t vc_all_gather_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
                                  vc_stream_t stream);
 
 /* Size of the device scratch array behind vc_all_reduce_decomposed_noalloc:
- * 32 MiB on every GPU that loads this library, held until the process exits. */
+ * 32 MiB on every GPU where that entry point has been called (or on every GPU
+ * the library's context is set up on, with eager module loading), held until
+ * the process exits. */
 #define VC_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* The decomposed AllReduce for callers that cannot allocate device memory.
@@ -358,7 +365,17 @@ vc_status_t vc_all_gather_bucket(const vc_bucket_tile_t *dev_tiles, int ntiles,
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.
+ * first call before any stream capture.  The array sits in a device-code
+ * module of its own.  With CUDA's lazy module loading (the default on Linux)
+ * that module, and with it the 32 MiB, is placed on a device only when it is
+ * first needed there: at this first call.  The memory then comes out of the
+ * device like any other allocation, so make the first call early, before a
+ * caching allocator has filled the GPU; a device that cannot hold the array
+ * makes the call return VC_ERR_CUDA.  (With eager loading,
+ * CUDA_MODULE_LOADING=EAGER, the array is placed when the library's CUDA
+ * context is set up.)  The cached address belongs to the device's primary
+ * context: after cudaDeviceReset it is stale, and this entry point must not
+ * be called again in that process.
  *
  * Sharing: every call uses the same array, which keeps the shards of the
  * last call.  Nothing in it needs to start at zero: the ReduceScatter writes
