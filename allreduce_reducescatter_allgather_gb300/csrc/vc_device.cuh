@@ -155,14 +155,16 @@ __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) {
 
 // 16-byte accesses with the default cache policy (measured faster on GB300
 // than the evict-first streaming hints for these access patterns).
-__device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+__host__ __device__ __forceinline__ uint4 ld16(const void* p) {
+    return *reinterpret_cast<const uint4*>(p);
+}
+__host__ __device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // 16 bytes at an address aligned only to the element size ES (a shard whose
 // start is not on a 16-byte boundary): the widest accesses the address
 // allows, 16, 8, 4 or 2 bytes.  Little-endian: byte 0 is the low byte of x.
 template <int ES>
-__device__ __forceinline__ void st_aligned(void* p, const uint4& v) {
+__host__ __device__ __forceinline__ void st_aligned(void* p, const uint4& v) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     if ((a & 15) == 0) {
         st16(p, v);
@@ -188,7 +190,7 @@ __device__ __forceinline__ void st_aligned(void* p, const uint4& v) {
 }
 
 template <int ES>
-__device__ __forceinline__ uint4 ld_aligned(const void* p) {
+__host__ __device__ __forceinline__ uint4 ld_aligned(const void* p) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     uint4 v;
     if ((a & 15) == 0) {
@@ -266,7 +268,7 @@ __device__ __forceinline__ uint4 shfl_down1(const uint4& v) {
 // Element k (of 16/ES) of v.  Called from fully unrolled loops, so k is a
 // constant after unrolling and the word index folds away.
 template <int ES>
-__device__ __forceinline__ unsigned long long elem_get(const uint4& v, int k) {
+__host__ __device__ __forceinline__ unsigned long long elem_get(const uint4& v, int k) {
     const unsigned w[4] = {v.x, v.y, v.z, v.w};
     if constexpr (ES == 2) return (w[k / 2] >> (16 * (k % 2))) & 0xffffu;
     else if constexpr (ES == 4) return w[k];
@@ -276,7 +278,7 @@ __device__ __forceinline__ unsigned long long elem_get(const uint4& v, int k) {
 // Stores bytes [from, from + len) of v at p (the destination of byte
 // `from`), one element at a time; from and len are multiples of ES.
 template <int ES>
-__device__ __forceinline__ void st_bytes(unsigned char* p, const uint4& v, int from, int len) {
+__host__ __device__ __forceinline__ void st_bytes(unsigned char* p, const uint4& v, int from, int len) {
 #pragma unroll
     for (int k = 0; k < 16 / ES; ++k) {
         const int b = k * ES;
@@ -297,7 +299,7 @@ __device__ __forceinline__ void st_bytes(unsigned char* p, const uint4& v, int f
 // byte positions of the result (the other bytes are zero), one element at a
 // time; from and to are multiples of ES.
 template <int ES>
-__device__ __forceinline__ uint4 ld_block_part(const unsigned char* blk, int from, int to) {
+__host__ __device__ __forceinline__ uint4 ld_block_part(const unsigned char* blk, int from, int to) {
     unsigned w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int k = 0; k < 16 / ES; ++k) {
@@ -426,8 +428,20 @@ __device__ __forceinline__ Vec<A, W> vop(const Vec<A, W>& a, const Vec<A, W>& b)
     return r;
 }
 
-// AVG: one division by n after the ordered sum.
-__device__ __forceinline__ float avg_div(float s, int n) { return __fdiv_rn(s, (float)n); }
+// AVG: one division by n after the ordered sum, correctly rounded.  For n a
+// power of two, 1/n = 2^-k is exact in binary, so s * 2^-k is the same real
+// number as s / n, and the correctly rounded product has the bits of the
+// correctly rounded quotient (subnormal results included; infinities stay
+// infinite): one multiply instead of a division.  Measured on GB300, the
+// bf16 ReduceScatter of a 25 MiB gradient bucket on eight ranks went from
+// 0.89x to 0.92x of the copy rate with AVG.  Other n divide.
+__device__ __forceinline__ float avg_div(float s, int n) {
+    if ((n & (n - 1)) == 0) {
+        const int k = __ffs(n) - 1;  // n = 2^k, 0 <= k <= 6
+        return __fmul_rn(s, __int_as_float((127 - k) << 23));
+    }
+    return __fdiv_rn(s, (float)n);
+}
 __device__ __forceinline__ long long avg_div(long long s, int n) { return s / (long long)n; }
 
 // ------------------------------------------------------------- loaders --
@@ -912,8 +926,9 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     }
 }
 
-// One vector slot on its own: the vector path if it lies inside one chunk
-// and inside the data on aligned bases, else element by element.
+// One vector slot on its own, in the kernels with a compile-time N: the
+// vector path if it lies inside one chunk and inside the data on aligned
+// bases, else element by element.
 template <class T, class Op, int ORDER, int NT, bool RS>
 __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
     constexpr int V = Traits<T>::V;
@@ -925,6 +940,78 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
         const int sel = (ORDER == kOrderDoubleTree) ? (i0 >= p.half) : c;
         auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
         store_result<T, NT, RS>(p, c, i0, acc, false);
+    } else {
+        for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
+    }
+}
+
+// One vector slot on its own, in the kernels with a run-time N (they stream
+// their operands in groups).  Inside the data on aligned bases, the N
+// operand vectors load as whole vectors and every lane's element is folded
+// at once, also when the vector straddles a chunk boundary (the ring folds
+// the two parts from two different ranks, a ReduceScatter stores them to two
+// shards) or the double binary tree's halfway point (two trees): the fold
+// then runs once per selector among the lanes (at most two, since q >= V
+// puts at most one chunk boundary in a vector, and there is one halfway
+// point), and each run stores the lanes it serves, element by element.
+// Element by element, each element's reduction waited for its own loads
+// group after group, and the few threads on straddling vectors ran many
+// microseconds after the rest of the grid (measured on GB300: bf16
+// ReduceScatter over twelve ranks with shards off the 16-byte grid, one SM
+// active 108 k cycles against 70 k on average, the call 47 % longer).  What
+// remains element by element: misaligned bases, the end of the data, the
+// padding, and shards shorter than a vector (tiny calls).
+// Inlined into the kernel: called as a separate function from the lanes of
+// a warp that leave the vector path while the others stay on it, it made
+// those other lanes' results wrong on GB300 (a ReduceScatter over 33 ranks:
+// every warp holding a straddling vector came out wrong; inlined, or called
+// by whole warps, every element was right; caught by the parity tests).
+// The kernels with a compile-time N keep the element path below: there
+// each element issues its loads in groups of up to 16 at once, and inlining
+// the vector path raised their registers (three blocks per SM down to two
+// at N = 3 and 5; two down to one at N = 16, 32, 64).
+template <class T, class Op, int ORDER, int NT, bool RS>
+__device__ __forceinline__ void reduce_slot_streaming(const ReduceParams& p, long long v) {
+    constexpr int V = Traits<T>::V;
+    using A = typename Traits<T>::Acc;
+    const long long i0 = v * V;
+    const int c = chunk_of(i0, p.q, p.inv_q, p.n);
+    const long long cut = (long long)(c + 1) * p.q;  // lanes from here are in chunk c + 1
+    const bool one_chunk = i0 + V <= cut;
+    if (p.vec_ok && i0 + V <= p.M && (one_chunk || p.q >= V)) {
+        // the fold's selector of element i in chunk ci: the ring's chunk,
+        // the double tree's half; the other orders fold every element alike
+        auto sel_of = [&](long long i, int ci) -> int {
+            if constexpr (ORDER == kOrderRing) return ci;
+            else if constexpr (ORDER == kOrderDoubleTree) return (int)(i >= p.half);
+            else return 0;
+        };
+        const int s0 = sel_of(i0, c);
+        const int s1 = sel_of(i0 + V - 1, one_chunk ? c : c + 1);
+        const bool whole = one_chunk && s0 == s1;
+        const VecLoader<T> ld{p, i0};
+#pragma unroll 1
+        for (int pass = 0; pass < (s1 != s0 ? 2 : 1); ++pass) {
+            const int sel = pass == 0 ? s0 : s1;
+            Vec<A, V> acc = fold<Op, ORDER, NT>(ld, p.n, sel);
+            if (whole) {
+                store_result<T, NT, RS>(p, c, i0, acc, false);
+                continue;
+            }
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const long long i = i0 + k;
+                const int ci = i >= cut ? c + 1 : c;
+                if (sel_of(i, ci) != sel) continue;
+                A r = acc.x[k];
+                if (p.avg) r = avg_div(r, p.n);
+                if constexpr (RS) {
+                    store1(static_cast<T*>(p.out[ci]) + (i - (long long)ci * p.q), r);
+                } else {
+                    for (int s = 0; s < p.nout; ++s) store1(static_cast<T*>(p.out[s]) + i, r);
+                }
+            }
+        }
     } else {
         for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
     }
@@ -944,7 +1031,8 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
 //    of the table (doubled when N is a run-time value, so a rotation never
 //    wraps), and so do the trees with a run-time N (tree B computes its
 //    rank indices).
-// Anything else goes slot by slot through reduce_slot.
+// Anything else goes slot by slot (reduce_slot, or reduce_slot_streaming
+// with a run-time N).
 template <class T, class Op, int ORDER, int NT, int U, bool RS>
 __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
     constexpr int V = Traits<T>::V;
@@ -1052,7 +1140,12 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
 #pragma unroll 1
             for (int u = 0; u < U; ++u) {
                 const long long v = v0 + (long long)u * blockDim.x;
-                if (v < nvec) reduce_slot<T, Op, ORDER, NT, RS>(p, v);
+                if (v < nvec) {
+                    if constexpr (NT > 0)
+                        reduce_slot<T, Op, ORDER, NT, RS>(p, v);
+                    else
+                        reduce_slot_streaming<T, Op, ORDER, NT, RS>(p, v);
+                }
             }
         }
     }
@@ -1126,12 +1219,20 @@ __device__ __noinline__ void gather_slot(const GatherParams& p, long long v, int
         const uint4 val = gather_load<ES>(p, s, i0);
         for (int r = r0; r < r1; ++r) st16(static_cast<U*>(p.out[r]) + i0, val);
     } else {
-        for (int k = 0; k < V && i0 + k < p.M; ++k) {
+        // every element's load first (they issue together), then the stores
+        U val[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
             const long long i = i0 + k;
-            const int si = chunk_of(i, p.q, p.inv_q, p.n);
-            const U val = static_cast<const U*>(p.in[si])[i - (long long)si * p.q];
-            for (int r = r0; r < r1; ++r) static_cast<U*>(p.out[r])[i] = val;
+            if (i < p.M) {
+                const int si = chunk_of(i, p.q, p.inv_q, p.n);
+                val[k] = static_cast<const U*>(p.in[si])[i - (long long)si * p.q];
+            }
         }
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            if (i0 + k < p.M)
+                for (int r = r0; r < r1; ++r) static_cast<U*>(p.out[r])[i0 + k] = val[k];
     }
 }
 

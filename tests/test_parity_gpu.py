@@ -554,36 +554,71 @@ def test_shards_off_the_vector_grid(env, dtype):
     the vector width, eight ranks, shard bases moved by 0 .. V-1 elements,
     inputs and outputs aligned), and q a whole number of vectors with only
     the bases moved; several warps per shard, a padded last shard; guards
-    before and after every shard and output."""
+    before and after every shard and output.  Also at three ranks (the
+    compile-time kernels with four vectors per thread) and twelve (the
+    kernel with a run-time N)."""
     vc, torch = env.vc, env.torch
     V = 16 // ESIZE[dtype]
-    n = 8
     k = 0
-    for q in (V * 301 + 1, V * 97 + V - 1, V * 160):
-        M = n * q - 3
-        for shift in range(V):
-            op = SWEEP_OPS[k % len(SWEEP_OPS)]
-            order = ORDERS[k % len(ORDERS)] if dtype in ("float32", "bfloat16") else "ring"
-            k += 1
-            xs = gen(dtype, n, M, seed=7100 + 13 * q + shift)
-            if op == "prod" and dtype in ("float32", "bfloat16"):
-                xs = gen_prod_floats(dtype, n, M)
-            d = to_device(torch, xs, dtype, env.dev)
-            z = Guarded(env, n, q, dtype, shift)
-            g = Guarded(env, n, M, dtype)
-            vc.vc_reduce_scatter(d, z.views, op=op, order=order)
-            vc.vc_all_gather(z.views, g.views)
-            torch.cuda.synchronize()
-            z.check_guards(env)
-            g.check_guards(env)
-            oz = oracle.reduce_scatter(xs, dtype, op, order)
-            zh = z.host()
-            og = oracle.all_gather(zh, M, dtype)
-            gh = g.host()
-            for r in range(n):
-                t = f"{dtype} {op} {order} q={q} shift={shift} rank {r}"
-                assert_bits_equal(zh[r], oz[r], dtype, "RS " + t)
-                assert_bits_equal(gh[r], og[r], dtype, "AG " + t)
+    # eight ranks: the compile-time kernels that preload their operands;
+    # three: the same with four vectors per thread; twelve: the kernel with
+    # a run-time N (one vector per thread, element-aligned pieces)
+    for n, q, shift in [(8, q, sh) for q in (V * 301 + 1, V * 97 + V - 1, V * 160)
+                        for sh in range(V)] + \
+                       [(n, q, sh) for n in (3, 12) for q in (V * 211 + 1, V * 53 + V - 1)
+                        for sh in range(V)]:
+        M = n * q - min(3, n - 1)  # ceil(M / n) = q
+        op = SWEEP_OPS[k % len(SWEEP_OPS)]
+        orders = orders_for(n)
+        order = orders[k % len(orders)] if dtype in ("float32", "bfloat16") else "ring"
+        k += 1
+        xs = gen(dtype, n, M, seed=7100 + 13 * q + shift)
+        if op == "prod" and dtype in ("float32", "bfloat16"):
+            xs = gen_prod_floats(dtype, n, M)
+        d = to_device(torch, xs, dtype, env.dev)
+        z = Guarded(env, n, q, dtype, shift)
+        g = Guarded(env, n, M, dtype)
+        vc.vc_reduce_scatter(d, z.views, op=op, order=order)
+        vc.vc_all_gather(z.views, g.views)
+        torch.cuda.synchronize()
+        z.check_guards(env)
+        g.check_guards(env)
+        oz = oracle.reduce_scatter(xs, dtype, op, order)
+        zh = z.host()
+        og = oracle.all_gather(zh, M, dtype)
+        gh = g.host()
+        for r in range(n):
+            t = f"{dtype} {op} {order} N={n} q={q} shift={shift} rank {r}"
+            assert_bits_equal(zh[r], oz[r], dtype, "RS " + t)
+            assert_bits_equal(gh[r], og[r], dtype, "AG " + t)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_avg_subnormal_quotients(env, dtype):
+    """AVG divides the ordered sum by N once.  For N a power of two the
+    kernels multiply by the exact reciprocal 2^-k instead; the correctly
+    rounded product and quotient are the same bits, including where the
+    result is subnormal.  Operands near the smallest normal fp32 (biased
+    exponents 1..9, both signs), so many quotients fall below it; every
+    path against the oracle's division, at power-of-two N and at N = 3, 12."""
+    vc, torch = env.vc, env.torch
+    rng = np.random.default_rng(17)
+    for n in (2, 3, 4, 8, 12, 16, 64):
+        M = 4099
+        xs = []
+        for _ in range(n):
+            bits = (rng.integers(1, 10, M, dtype=np.uint32) << 23) \
+                | rng.integers(0, 1 << 23, M, dtype=np.uint32) \
+                | (rng.integers(0, 2, M, dtype=np.uint32) << 31)
+            f = bits.view(np.float32)
+            xs.append(f if dtype == "float32" else oracle.bf16_round(f))
+        for order in orders_for(n):
+            res = run_all_paths(env, xs, dtype, "avg", order)
+            check_all_paths(res, xs, dtype, "avg", order, tag=f"subnormal N={n}")
+        oy = oracle.all_reduce(xs, dtype, "avg", "ring")
+        as_f = oy[0].view(np.float32) if dtype == "float32" else \
+            (oy[0].astype(np.uint32) << 16).view(np.float32)
+        assert np.count_nonzero((as_f != 0) & (np.abs(as_f) < np.finfo(np.float32).tiny)) > 20
 
 
 def test_all_gather_from_arbitrary_shards(env):
