@@ -946,8 +946,9 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
 }
 
 // One vector slot on its own, in the kernels with a run-time N (they stream
-// their operands in groups).  Inside the data on aligned bases, the N
-// operand vectors load as whole vectors and every lane's element is folded
+// their operands in groups, through the pointer table in shared memory).
+// Inside the data on aligned bases, the N operand vectors load as whole
+// vectors, in the vector path's groups, and every lane's element is folded
 // at once, also when the vector straddles a chunk boundary (the ring folds
 // the two parts from two different ranks, a ReduceScatter stores them to two
 // shards) or the double binary tree's halfway point (two trees): the fold
@@ -971,7 +972,9 @@ __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
 // the vector path raised their registers (three blocks per SM down to two
 // at N = 3 and 5; two down to one at N = 16, 32, 64).
 template <class T, class Op, int ORDER, int NT, bool RS>
-__device__ __forceinline__ void reduce_slot_streaming(const ReduceParams& p, long long v) {
+__device__ __forceinline__ void reduce_slot_streaming(const ReduceParams& p, const void* const* s_in,
+                                                      long long v) {
+    static_assert(NT <= 0, "the kernels with a run-time N only");
     constexpr int V = Traits<T>::V;
     using A = typename Traits<T>::Acc;
     const long long i0 = v * V;
@@ -989,11 +992,17 @@ __device__ __forceinline__ void reduce_slot_streaming(const ReduceParams& p, lon
         const int s0 = sel_of(i0, c);
         const int s1 = sel_of(i0 + V - 1, one_chunk ? c : c + 1);
         const bool whole = one_chunk && s0 == s1;
-        const VecLoader<T> ld{p, i0};
+        // the pointer table in shared memory, as the vector path reads it
+        // (doubled for the ring, so its folds run in groups of 16 unwrapped)
+        const SharedTableLoader<T> ld{s_in, i0};
 #pragma unroll 1
         for (int pass = 0; pass < (s1 != s0 ? 2 : 1); ++pass) {
             const int sel = pass == 0 ? s0 : s1;
-            Vec<A, V> acc = fold<Op, ORDER, NT>(ld, p.n, sel);
+            Vec<A, V> acc;
+            if constexpr (ORDER == kOrderRing)
+                acc = fold_ring_doubled<Op>(ld, p.n, sel);
+            else
+                acc = fold<Op, ORDER, NT>(ld, p.n, sel);
             if (whole) {
                 store_result<T, NT, RS>(p, c, i0, acc, false);
                 continue;
@@ -1144,7 +1153,7 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
                     if constexpr (NT > 0)
                         reduce_slot<T, Op, ORDER, NT, RS>(p, v);
                     else
-                        reduce_slot_streaming<T, Op, ORDER, NT, RS>(p, v);
+                        reduce_slot_streaming<T, Op, ORDER, NT, RS>(p, s_in, v);
                 }
             }
         }
