@@ -16,9 +16,26 @@ The step moves 4*N*M*s + 2*M*s bytes; value = those bytes / step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+Beside the headline the line carries (one GPU only):
+  configs               every workload: the worked example, 8 x 1,000,003
+                        fp32, the 25 MiB bf16 bucket, 4 x 256 MiB fp32 and
+                        4 x 512 MiB int64, and a 64 MiB / 1 GiB per rank
+                        summary of the size x rank-count sweep.  Each path
+                        with per-call median / P95 / CV (path order
+                        alternating each cycle), algorithmic bytes, GB/s and
+                        fraction of the copy peak, and an oracle check of
+                        that run's outputs (every element, or sampled
+                        indices with every chunk boundary at full size);
+  direct_vs_decomposed  single calls and CUDA-graph loops of 16 calls from
+                        1 KiB to 256 MiB per rank;
+  e2e                   the step from pinned host buffers, with the host
+                        link probed in the same run;
+  memory_mib, gradient_buckets, cpu_baseline, cpu_baseline_all_cores.
+
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (the path shards by index range with no exchange; weak scaling), the step
-time is the max over ranks, and value counts the bytes of all ranks.
+time is the max over ranks, and value counts the bytes of all ranks.  The
+ranks talk only over a host-side gloo group (a barrier, a max and a sum).
 --impl reference times the CPU oracle instead, on a bounded window of the
 same workload (rank 0 only).
 """
@@ -175,14 +192,13 @@ def dist_info():
 
 
 def aggregate(torch, local_ms: float, local_bytes: int, world: int):
-    """Max step time and total bytes over ranks (control plane only)."""
+    """Max step time and total bytes over ranks (control plane only: two
+    host scalars over the gloo process group; no GPU collective)."""
     if world == 1:
         return local_ms, local_bytes
     import torch.distributed as dist
-    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() \
-        else torch.device("cpu")
-    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
-    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(b, op=dist.ReduceOp.SUM)
     return float(t.item()), int(b.item())
@@ -375,10 +391,12 @@ def run_ours(args, workload: dict):
         import datetime
 
         import torch.distributed as dist
-        # a rank that dies or never arrives ends the others' next collective
-        # with an error after this long, instead of leaving them waiting
-        dist.init_process_group("nccl", device_id=dev,
-                                timeout=datetime.timedelta(seconds=args.dist_timeout))
+        # The control plane (a barrier around the timed region and the
+        # max / sum of two scalars) runs on the host over gloo: the ranks
+        # exchange no data, so no GPU collective library is involved.  A rank
+        # that dies or never arrives ends the others' next collective with an
+        # error after this long, instead of leaving them waiting.
+        dist.init_process_group("gloo", timeout=datetime.timedelta(seconds=args.dist_timeout))
 
     w = dict(workload)
     n, M, dtype = w.pop("n"), w.pop("M"), w.pop("dtype")
@@ -472,10 +490,15 @@ def run_ours(args, workload: dict):
                             if M == si.WORKLOADS[args.workload]["M"] else None),
                 "algorithmic_bytes_per_launch": by["fused_ar"]}
 
+    del y, y2, sh
+    torch.cuda.empty_cache()
     memory = memory_report(torch, vc, d, args, dev) if not args.no_memory else None
     buckets = bucket_report(torch, vc, args, dev) if not args.no_memory else None
-    latency = latency_table(torch, vc, args, dev) if not args.no_memory else None
-    e2e = e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, by["step"])
+    latency = latency_table(torch, vc, args, dev, peak) if not args.no_memory else None
+    e2e = e2e_measure(torch, vc, d, args, dev, stream, by["step"])
+    configs = (configs_report(torch, vc, args, dev, stream, peak, d, memory)
+               if (world == 1 and not args.no_configs
+                   and M == si.WORKLOADS[args.workload]["M"]) else None)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -497,6 +520,8 @@ def run_ours(args, workload: dict):
         line["gradient_buckets"] = buckets
     if latency is not None:
         line["direct_vs_decomposed"] = latency
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         g, steps, secs = time_oracle(workload, args.op, args.order, args.cpu_seconds,
                                      window=1 << 22)
@@ -509,13 +534,14 @@ def run_ours(args, workload: dict):
         try:
             gp, cores, psteps, psecs = time_oracle_all_cores(workload, args.op, args.order,
                                                             args.cpu_seconds, window=1 << 22)
-            line["cpu_baseline"]["all_cores"] = {
+            line["cpu_baseline_all_cores"] = {
                 "value": round(gp, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "cpu": line["cpu_baseline"]["cpu"],
                 "sample": f"{psteps} oracle steps in {cores} spawned processes, each on its "
                           f"own {min(1 << 22, M)}-element window of every rank, "
                           f"{psecs:.1f} s"}
         except Exception as e:  # the single-core figure above still stands
-            line["cpu_baseline"]["all_cores"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+            line["cpu_baseline_all_cores"] = {"error": f"{type(e).__name__}: {e}"[:200]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -523,49 +549,103 @@ def run_ours(args, workload: dict):
     return 0
 
 
-def e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, step_bytes_):
+def link_probe(torch, dev, nbytes: int = 1 << 30, reps: int = 3) -> dict:
+    """The host link in this run: pinned 1 GiB host-to-device and device-to-
+    host copies alone, and both at once on two streams (best of `reps`, CUDA
+    events), in GB/s."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    h_in.fill_(1)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(kind):
+        out = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(s1)
+            if kind in ("h2d", "both"):
+                with torch.cuda.stream(s1):
+                    d_a.copy_(h_in, non_blocking=True)
+            if kind in ("d2h", "both"):
+                s2.wait_event(a)
+                with torch.cuda.stream(s2):
+                    h_out.copy_(d_b, non_blocking=True)
+                s1.wait_stream(s2)
+            b.record(s1)
+            b.synchronize()
+            moved = nbytes * (2 if kind == "both" else 1)
+            out.append(moved / (a.elapsed_time(b) / 1e3) / 1e9)
+        return round(max(out), 1)
+
+    res = {"h2d_gbs": best("h2d"), "d2h_gbs": best("d2h"), "both_gbs": best("both"),
+           "bytes": nbytes, "how": f"pinned {nbytes >> 20} MiB copies, best of {reps}"}
+    del h_in, h_out, d_a, d_b
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e_measure(torch, vc, d, args, dev, stream, step_bytes_):
     """The same step through the public API with the inputs in pinned host
     memory: each step copies the N inputs in, runs both AllReduce paths and
-    copies every output of both back.  Steps are pipelined the way a user
-    would run them: two sets of device buffers and of host outputs, one
-    stream per direction, so step k+1's inputs travel while step k's
-    outputs come back (the two link directions run concurrently)."""
-    n = len(d)
-    host_in = [t.cpu().pin_memory() for t in d]
-    sets = [(d, y, y2, sh),
-            ([torch.empty_like(t) for t in d], [torch.empty_like(t) for t in d],
-             [torch.empty_like(t) for t in d], [torch.empty_like(t) for t in sh])]
-    host_out = [([torch.empty_like(t, device="cpu").pin_memory() for t in d],
-                 [torch.empty_like(t, device="cpu").pin_memory() for t in d]) for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    copies every output of both back.  Each buffer set's N rank buffers are
+    views of one contiguous allocation (host and device alike), so a step
+    issues one host-to-device copy and two device-to-host copies (the fused
+    and the decomposed outputs).  Steps are pipelined the way a user would
+    run them: two sets of device buffers and of host outputs, one stream per
+    direction, so step k+1's inputs travel while step k's outputs come back.
+    The host link is probed in the same run, and the step's host traffic is
+    reported as a fraction of the both-directions rate."""
+    n, M = len(d), d[0].numel()
+    dt = d[0].dtype
+    q = vc.vc_shard_count(M, n)
+    link = link_probe(torch, dev)
+    host_in = torch.empty(n * M, dtype=dt, pin_memory=True)
+    for r in range(n):
+        host_in[r * M:(r + 1) * M].copy_(d[r])
+
+    def views(flat, count):
+        return [flat[r * count:(r + 1) * count] for r in range(n)]
+
+    sets = []
+    for _ in range(2):
+        flat = [torch.empty(n * M, dtype=dt, device=dev) for _ in range(3)]
+        sh = torch.empty(n * q, dtype=dt, device=dev)
+        sets.append((flat, views(flat[0], M), views(flat[1], M), views(sh, q), views(flat[2], M)))
+    host_out = [(torch.empty(n * M, dtype=dt, pin_memory=True),
+                 torch.empty(n * M, dtype=dt, pin_memory=True)) for _ in range(2)]
+    h2d = host_in.numel() * host_in.element_size()
     d2h = 2 * h2d
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    calls = [(vc.prepare_all_reduce(di, dy, op=args.op, order=args.order),
+              vc.prepare_all_reduce_decomposed(di, dsh, dy2, op=args.op, order=args.order))
+             for _, di, dy, dsh, dy2 in sets]
 
     def run(steps):
         for k in range(steps):
             j = k % 2
-            di, dy, dy2, dsh = sets[j]
+            flat = sets[j][0]
             hy, hy2 = host_out[j]
             if k >= 2:
                 s_in.wait_event(comp_done[j])  # set j's inputs no longer read
             with torch.cuda.stream(s_in):
-                for r in range(n):
-                    di[r].copy_(host_in[r], non_blocking=True)
+                flat[0].copy_(host_in, non_blocking=True)
             in_ready[j].record(s_in)
             stream.wait_event(in_ready[j])
             if k >= 2:
                 stream.wait_event(out_done[j])  # set j's outputs already copied out
-            vc.vc_all_reduce(di, dy, op=args.op, order=args.order, stream=stream)
-            vc.vc_all_reduce_decomposed(di, dsh, dy2, op=args.op, order=args.order,
-                                        stream=stream)
+            ar, dec = calls[j]
+            ar(stream=stream)
+            dec(stream=stream)
             comp_done[j].record(stream)
             s_out.wait_event(comp_done[j])
             with torch.cuda.stream(s_out):
-                for r in range(n):
-                    hy[r].copy_(dy[r], non_blocking=True)
-                    hy2[r].copy_(dy2[r], non_blocking=True)
+                hy.copy_(flat[1], non_blocking=True)
+                hy2.copy_(flat[2], non_blocking=True)
             out_done[j].record(s_out)
 
     run(2)
@@ -581,14 +661,21 @@ def e2e_measure(torch, vc, d, y, y2, sh, args, dev, stream, step_bytes_):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.e2e_steps
     wall_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
-    # every output of the last step came back intact
-    ref = sets[(args.e2e_steps - 1) % 2][1][0].cpu()
-    assert torch.equal(host_out[(args.e2e_steps - 1) % 2][0][n - 1], ref)
-    del sets, host_out
+    # the last step's outputs came back intact: both paths, every rank
+    last = (args.e2e_steps - 1) % 2
+    assert torch.equal(host_out[last][0], sets[last][0][1].cpu())
+    assert torch.equal(host_out[last][1], sets[last][0][2].cpu())
+    del sets, host_out, calls
+    torch.cuda.empty_cache()
+    host_gbs = (h2d + d2h) / (ms / 1e3) / 1e9
+    link["e2e_host_gbs"] = round(host_gbs, 1)
+    link["e2e_frac_of_both"] = round(host_gbs / link["both_gbs"], 4) if link["both_gbs"] else None
+    serial_ms = (h2d / link["h2d_gbs"] + d2h / link["d2h_gbs"]) / 1e6
+    link["serial_link_ms_per_step"] = round(serial_ms, 3)
     return {"value": round(step_bytes_ / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "host_wall_ms_per_step": round(wall_ms, 3), "steps": args.e2e_steps,
-            "pipelined": True}
+            "pipelined": True, "copies_per_step": {"h2d": 1, "d2h": 2}, "link": link}
 
 
 def memory_report(torch, vc, d, args, dev):
@@ -670,76 +757,525 @@ def memory_report(torch, vc, d, args, dev):
     return out
 
 
-def latency_table(torch, vc, args, dev):
+def latency_table(torch, vc, args, dev, peak, K: int = 16):
     """p1's direct-vs-decomposed experiment on four virtual ranks ("NCCL 专家
     课程 07", 性能实验为什么交替执行顺序 / 严格处理不稳定点): per-rank sizes 1 KiB,
-    64 KiB, 1 MiB, 16 MiB, 256 MiB of fp32; 3 warm-ups, then 10 cycles that
-    alternate which path runs first; inputs reset and synchronised outside
-    each timed call; median / P95 / CV of the per-call CUDA-event times; the
-    decomposed / direct ratio is given only when both CVs are at most 5 %."""
-    import numpy as np
+    64 KiB, 1 MiB, 16 MiB, 256 MiB of fp32, out of place (the inputs never
+    change, so no reset is needed); 3 warm-ups, then 10 cycles that
+    alternate which path runs first; median / P95 / CV per path; the
+    decomposed / direct ratio only when both CVs are at most 5 %.  Two
+    timings per size:
+      single  one call per event pair, after an L2-evicting read that keeps
+              the GPU busy while the host issues the call (device time of one
+              call, launch included);
+      graph   a CUDA graph of K back-to-back calls per event pair, the time
+              divided by K (what a loop of calls costs per call; the host's
+              per-call jitter does not enter)."""
     n = 4
     stream = torch.cuda.current_stream(dev)
+    single = CallTimer(torch, dev, stream)
+    plain = CallTimer(torch, dev, stream, evict=False)
     rows = []
     for nbytes in (1 << 10, 64 << 10, 1 << 20, 16 << 20, 256 << 20):
         M = nbytes // 4
         g = torch.Generator(device=dev)
         g.manual_seed(nbytes)
-        base = [torch.randn(M, generator=g, device=dev) for _ in range(n)]
-        work = [t.clone() for t in base]
+        x = [torch.randn(M, generator=g, device=dev) for _ in range(n)]
+        y = [torch.empty_like(t) for t in x]
+        y2 = [torch.empty_like(t) for t in x]
         shards = [torch.empty(vc.vc_shard_count(M, n), device=dev) for _ in range(n)]
-
-        def reset():
-            for w, b in zip(work, base):
-                w.copy_(b)
-            torch.cuda.synchronize()
-
-        # prepared calls: checked once, one C call each (the first C call on
-        # the stream, as a user with persistent buffers would issue it)
-        ar = vc.prepare_all_reduce(work, None, op=args.op, order=args.order)
-        dec = vc.prepare_all_reduce_decomposed(work, shards, None, op=args.op,
-                                               order=args.order)
-
-        def direct():
-            ar(stream=stream)
-
-        def decomposed():
-            dec(stream=stream)
-
-        def timed(fn):
-            reset()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            b.synchronize()
-            return a.elapsed_time(b) * 1e3  # µs
-
-        for _ in range(3):
-            timed(direct)
-            timed(decomposed)
-        t = {"direct": [], "decomposed": []}
-        for cycle in range(10):
-            order = ("direct", "decomposed") if cycle % 2 == 0 else ("decomposed", "direct")
-            for mode in order:
-                t[mode].append(timed(direct if mode == "direct" else decomposed))
+        ar = vc.prepare_all_reduce(x, y, op=args.op, order=args.order)
+        dec = vc.prepare_all_reduce_decomposed(x, shards, y2, op=args.op, order=args.order)
+        b = step_bytes(n, M, 4)
         row = {"bytes_per_rank": nbytes}
-        for mode, v in t.items():
-            a = np.array(v)
-            med = float(np.median(a))
-            row[mode] = {"median_us": round(med, 3), "p95_us": round(float(np.percentile(a, 95)), 3),
-                         "cv": round(float(a.std() / a.mean()), 4),
-                         "payload_gbs": round(nbytes * n / med / 1e3, 2),
-                         "hbm_gbs": round(step_bytes(n, M, 4)["fused_ar" if mode == "direct"
-                                                               else "decomposed_ar"] / med / 1e3, 1)}
-        stable = row["direct"]["cv"] <= 0.05 and row["decomposed"]["cv"] <= 0.05
-        row["decomposed_over_direct"] = (round(row["decomposed"]["median_us"]
-                                               / row["direct"]["median_us"], 3)
-                                         if stable else "unstable")
+
+        def finish(t, scale):
+            r = {"direct": call_stats([v / scale for v in t["direct"]], b["fused_ar"], peak),
+                 "decomposed": call_stats([v / scale for v in t["decomposed"]],
+                                          b["decomposed_ar"], peak)}
+            for mode in ("direct", "decomposed"):
+                r[mode]["payload_gbs"] = round(nbytes * n / r[mode]["median_us"] / 1e3, 2)
+            stable = r["direct"]["stable"] and r["decomposed"]["stable"]
+            r["decomposed_over_direct"] = (round(r["decomposed"]["median_us"]
+                                                 / r["direct"]["median_us"], 3)
+                                           if stable else "unstable")
+            return r
+
+        row["single"] = finish(single.alternating([("direct", lambda: ar(stream=stream)),
+                                                   ("decomposed", lambda: dec(stream=stream))]), 1)
+        graphs = {name: graph_loop(torch, fn, K) for name, fn in (("direct", ar),
+                                                                   ("decomposed", dec))}
+        row["graph"] = finish(plain.alternating([("direct", graphs["direct"].replay),
+                                                 ("decomposed", graphs["decomposed"].replay)]), K)
+        row["graph"]["calls_per_replay"] = K
         rows.append(row)
-        del base, work, shards, ar, dec
+        del x, y, y2, shards, ar, dec, graphs
     torch.cuda.empty_cache()
     return rows
+
+
+# ------------------------------------------------- every configuration --
+
+class CallTimer:
+    """Per-call CUDA-event times on one stream, the method of "NCCL 专家课程
+    07", 性能实验: warm-ups, then cycles in which the order of the paths
+    alternates (forward on even cycles, reversed on odd ones).  Before every
+    timed call a read of twice the L2 evicts the last call's data (so small
+    configurations are timed from HBM too) and keeps the GPU busy while the
+    host issues the call, so the events time the call on the device, launch
+    included, without the host's time to reach it.  (A read leaves the lines
+    clean; an evicting write would leave dirty lines for the timed call to
+    write back.)"""
+
+    def __init__(self, torch, dev, stream, evict: bool = True):
+        self.torch, self.stream = torch, stream
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = (torch.ones(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+                      if evict else None)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def alternating(self, paths, cycles: int = 10, warmup: int = 3) -> dict:
+        """paths: [(name, fn)], each fn issuing one call on the stream.
+        Returns {name: [ms per call, one per cycle]}."""
+        torch = self.torch
+        for _ in range(warmup):
+            for _, fn in paths:
+                fn()
+        torch.cuda.synchronize()
+        out = {name: [] for name, _ in paths}
+        for k in range(cycles):
+            seq = paths if k % 2 == 0 else paths[::-1]
+            evs = []
+            for name, fn in seq:
+                if self.flush is not None:
+                    torch.sum(self.flush, dim=0, out=self.sink)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+                evs.append((name, a, b))
+            torch.cuda.synchronize()
+            for name, a, b in evs:
+                out[name].append(a.elapsed_time(b))
+        return out
+
+
+def graph_loop(torch, fn, K: int):
+    """fn (one call on the current stream) captured K times back to back in
+    a CUDA graph; returns the graph's replay (one launch of K calls)."""
+    fn()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for _ in range(K):
+            fn()
+    return gr
+
+
+def call_stats(ms: list, nbytes: int, peak: float) -> dict:
+    """Median / P95 / CV of per-call times, and the median's HBM rate
+    against the copy peak.  "stable" (CV <= 5 %) marks the figures a ratio
+    may be claimed from ("NCCL 专家课程 07", 严格处理不稳定点)."""
+    import numpy as np
+    a = np.asarray(ms, dtype=np.float64)
+    med = float(np.median(a))
+    g = nbytes / (med / 1e3) / 1e9
+    cv = float(a.std() / a.mean()) if a.mean() > 0 else 0.0
+    return {"median_us": round(med * 1e3, 2), "p95_us": round(float(np.percentile(a, 95)) * 1e3, 2),
+            "cv": round(cv, 4), "calls": int(a.size), "bytes": int(nbytes), "gbs": round(g, 1),
+            "frac": round(g / peak, 4), "stable": cv <= 0.05}
+
+
+def host_bits(t, dtype: str):
+    """A device tensor's bytes as a numpy array of the oracle's storage type
+    (bf16 as raw uint16 bits)."""
+    import numpy as np
+    if dtype == "bfloat16":
+        import torch
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _bits(a):
+    import numpy as np
+    a = np.ascontiguousarray(a)
+    return a.view({1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}[a.itemsize])
+
+
+class Check:
+    """Bitwise comparison of GPU outputs with the oracle, counted."""
+
+    def __init__(self, kind: str):
+        self.kind, self.compared, self.mismatches, self.outputs = kind, 0, 0, set()
+
+    def eq(self, name: str, got, want):
+        import numpy as np
+        g, w = _bits(got), _bits(want)
+        self.outputs.add(name)
+        self.compared += int(w.size)
+        self.mismatches += int(np.count_nonzero(g != w)) if g.shape == w.shape else int(w.size)
+
+    def summary(self, **extra) -> dict:
+        return {"kind": self.kind, "outputs": sorted(self.outputs), "elements": self.compared,
+                "mismatches": self.mismatches, "bit_exact": self.mismatches == 0, **extra}
+
+
+def sample_indices(M: int, n: int, q: int, k: int = 4096, seed: int = 0):
+    """k random indices of [0, M) plus both sides of every chunk boundary
+    and the two ends, sorted."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    idx = set(int(i) for i in rng.integers(0, M, size=min(k, M)))
+    for c in range(1, n):
+        for i in (c * q - 1, c * q):
+            if 0 <= i < M:
+                idx.add(i)
+    idx.update((0, M - 1))
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def sampled_operands(torch, d, idx, dtype):
+    """Every rank's operand at the sampled indices, read from the device."""
+    it = torch.from_numpy(idx).to(d[0].device)
+    return [host_bits(t[it], dtype) for t in d]
+
+
+def check_rs_sampled(chk, torch, z, idx, want, n, M, q, dtype, op, name="RS"):
+    """Shard c = floor(i/q) at i - cq against the oracle's value at i, and
+    the padded tail of the last shard against the op's identity (0 for AVG)."""
+    import numpy as np
+    import oracle
+    for c in range(n):
+        sel = np.flatnonzero((idx // q) == c)
+        if sel.size == 0:
+            continue
+        off = torch.from_numpy(idx[sel] - c * q).to(z[c].device)
+        chk.eq(name, host_bits(z[c][off], dtype), want[sel])
+    tail = n * q - M
+    if tail > 0:
+        e = np.zeros(1, oracle.NP_STORAGE[dtype]) if op == "avg" else \
+            np.full(1, oracle.identity(dtype, op), oracle.NP_STORAGE[dtype])
+        chk.eq(name + " padding", host_bits(z[n - 1][q - tail:], dtype), np.repeat(e, tail))
+
+
+def check_full_sampled(chk, torch, name, outs, idx, want, dtype):
+    """Every output tensor at the sampled indices."""
+    it = torch.from_numpy(idx).to(outs[0].device)
+    for t in outs:
+        chk.eq(name, host_bits(t[it], dtype), want)
+
+
+def config_c1(torch, vc, dev, stream, peak):
+    """The pages' worked example: four ranks, twenty int64, x = 100r + i.
+    SUM (600 + 4i, shards of five) and MAX (300 + i), ring order, direct
+    AllReduce against ReduceScatter + AllGather, every output against the
+    oracle and the closed forms; the two negative checks must fail (a rolled
+    gather, and MAX with zero padding on M = 19 all-negative inputs).  Tiny:
+    latency only."""
+    import numpy as np
+    import oracle
+    import synthetic_inputs as si
+    n, M = 4, 20
+    xs = si.generate("int64", "rank_linear", n, M, seed=0)
+    d = [torch.from_numpy(x.copy()).to(dev) for x in xs]
+    q = vc.vc_shard_count(M, n)
+    chk = Check("full")
+    timer = CallTimer(torch, dev, stream)
+    loops = CallTimer(torch, dev, stream, evict=False)
+    K = 16
+    out = {"config": "N=4, M=20 int64, x = 100r + i; SUM and MAX; ring; direct AR vs RS+AG",
+           "q": q, "timing": "single: one call per event pair after an L2-evicting read; "
+                             f"graph: {K} calls per CUDA-graph replay, time / {K}", "ops": {}}
+    closed = {"sum": 600 + 4 * np.arange(M), "max": 300 + np.arange(M)}
+    for op in ("sum", "max"):
+        y = [torch.empty_like(t) for t in d]
+        z = [torch.empty(q, dtype=torch.int64, device=dev) for _ in range(n)]
+        g = [torch.empty_like(t) for t in d]
+        ar = vc.prepare_all_reduce(d, y, op=op, order="ring")
+        rs = vc.prepare_reduce_scatter(d, z, op=op, order="ring")
+        ag = vc.prepare_all_gather(z, g)
+        dec = vc.prepare_all_reduce_decomposed(d, [torch.empty_like(t) for t in z], g,
+                                               op=op, order="ring")
+        ar(stream=stream)
+        rs(stream=stream)
+        ag(stream=stream)
+        torch.cuda.synchronize()
+        oy = oracle.all_reduce(xs, "int64", op, "ring")
+        oz = oracle.reduce_scatter(xs, "int64", op, "ring")
+        for r in range(n):
+            chk.eq("AR", y[r].cpu().numpy(), oy[r])
+            chk.eq("AR closed form", y[r].cpu().numpy(), closed[op])
+            chk.eq("RS", z[r].cpu().numpy(), oz[r])
+            chk.eq("RS+AG", g[r].cpu().numpy(), oy[r])
+        t = timer.alternating([("all_reduce", lambda: ar(stream=stream)),
+                               ("rs_then_ag", lambda: dec(stream=stream))])
+        gl = {k: graph_loop(torch, f, K) for k, f in (("all_reduce", ar), ("rs_then_ag", dec))}
+        tg = loops.alternating([(k, g.replay) for k, g in gl.items()])
+        b = step_bytes(n, M, 8)
+        out["ops"][op] = {
+            "single": {"all_reduce": call_stats(t["all_reduce"], b["fused_ar"], peak),
+                       "rs_then_ag": call_stats(t["rs_then_ag"], b["decomposed_ar"], peak)},
+            "graph": {"all_reduce": call_stats([v / K for v in tg["all_reduce"]],
+                                               b["fused_ar"], peak),
+                      "rs_then_ag": call_stats([v / K for v in tg["rs_then_ag"]],
+                                               b["decomposed_ar"], peak)}}
+        del gl
+    # negative checks: a gather whose shards are rolled by one rank, and MAX
+    # shards padded with zero instead of the identity, must both be caught
+    z = [torch.empty(q, dtype=torch.int64, device=dev) for _ in range(n)]
+    vc.vc_reduce_scatter(d, z, op="sum")
+    rolled = [torch.empty_like(t) for t in d]
+    vc.vc_all_gather(z[1:] + z[:1], rolled)
+    torch.cuda.synchronize()
+    oy = oracle.all_reduce(xs, "int64", "sum", "ring")
+    rolled_caught = any(not np.array_equal(rolled[r].cpu().numpy(), oy[r]) for r in range(n))
+    M2 = 19
+    xneg = [-(100 * r + np.arange(M2, dtype=np.int64)) - 1 for r in range(n)]
+    dn = [torch.from_numpy(x).to(dev) for x in xneg]
+    q2 = vc.vc_shard_count(M2, n)
+    zn = [torch.empty(q2, dtype=torch.int64, device=dev) for _ in range(n)]
+    vc.vc_reduce_scatter(dn, zn, op="max")
+    torch.cuda.synchronize()
+    oz = oracle.reduce_scatter(xneg, "int64", "max", "ring")
+    for r in range(n):
+        chk.eq("RS (M=19, MAX, identity padding)", zn[r].cpu().numpy(), oz[r])
+    # the same shards with the padding slot filled with 0 instead of MAX's
+    # identity: the comparator must tell them from the GPU's shards
+    zero_pad = [o.copy() for o in oz]
+    zero_pad[n - 1][q2 - (n * q2 - M2):] = 0
+    zero_pad_caught = any(not np.array_equal(zn[r].cpu().numpy(), zero_pad[r]) for r in range(n))
+    out["negatives"] = {"rolled_gather_caught": bool(rolled_caught),
+                        "max_zero_padding_caught": bool(zero_pad_caught)}
+    out["oracle_check"] = chk.summary()
+    return out
+
+
+def config_c2(torch, vc, dev, stream, peak):
+    """Eight ranks of 1,000,003 fp32 uniform[-1, 1) (q = 125,001, five
+    padding slots): SUM / MAX / MIN x ring / recursive halving x RS, AG, fused
+    AR and decomposed AR, every output against the oracle, element by
+    element.  The 30.5 MiB of inputs fit in L2: every timed call follows an
+    L2-evicting read."""
+    import oracle
+    import synthetic_inputs as si
+    w = si.WORKLOADS["n8_m1000003_f32_uniform"]
+    n, M = w["n"], w["M"]
+    xs = si.generate("float32", w["dist"], n, M, seed=w["seed"])
+    d = [torch.from_numpy(x).to(dev) for x in xs]
+    q = vc.vc_shard_count(M, n)
+    z = [torch.empty(q, device=dev) for _ in range(n)]
+    g = [torch.empty(M, device=dev) for _ in range(n)]
+    y = [torch.empty(M, device=dev) for _ in range(n)]
+    s2 = [torch.empty(q, device=dev) for _ in range(n)]
+    y2 = [torch.empty(M, device=dev) for _ in range(n)]
+    timer = CallTimer(torch, dev, stream)
+    b = step_bytes(n, M, 4)
+    chk = Check("full")
+    out = {"config": "N=8, M=1,000,003 fp32 uniform[-1,1); SUM/MAX/MIN x ring/RH; "
+                     "RS, AG, AR, decomposed; trimmed to M", "q": q, "cases": {}}
+    for order in ("ring", "recursive_halving"):
+        for op in ("sum", "max", "min"):
+            rs = vc.prepare_reduce_scatter(d, z, op=op, order=order)
+            ag = vc.prepare_all_gather(z, g)
+            ar = vc.prepare_all_reduce(d, y, op=op, order=order)
+            dec = vc.prepare_all_reduce_decomposed(d, s2, y2, op=op, order=order)
+            t = timer.alternating([("reduce_scatter", lambda: rs(stream=stream)),
+                                   ("all_gather", lambda: ag(stream=stream)),
+                                   ("all_reduce", lambda: ar(stream=stream)),
+                                   ("decomposed_ar", lambda: dec(stream=stream))])
+            torch.cuda.synchronize()
+            oz = oracle.reduce_scatter(xs, "float32", op, order)
+            oy = oracle.all_reduce(xs, "float32", op, order)
+            for r in range(n):
+                chk.eq("RS", host_bits(z[r], "float32"), oz[r])
+                chk.eq("AG", host_bits(g[r], "float32"), oy[r])
+                chk.eq("AR", host_bits(y[r], "float32"), oy[r])
+                chk.eq("decomposed shards", host_bits(s2[r], "float32"), oz[r])
+                chk.eq("decomposed AR", host_bits(y2[r], "float32"), oy[r])
+            out["cases"][f"{op}/{order}"] = {
+                "reduce_scatter": call_stats(t["reduce_scatter"], b["reduce_scatter"], peak),
+                "all_gather": call_stats(t["all_gather"], b["all_gather"], peak),
+                "all_reduce": call_stats(t["all_reduce"], b["fused_ar"], peak),
+                "decomposed_ar": call_stats(t["decomposed_ar"], b["decomposed_ar"], peak)}
+    out["oracle_check"] = chk.summary()
+    return out
+
+
+def config_c3(torch, vc, dev, stream, peak):
+    """One 25 MiB gradient bucket on eight ranks: 13,107,200 bf16 normal(0,
+    1e-3) each, SUM then AVG with fp32 accumulation, ring order; the ZeRO
+    ReduceScatter (shards only) and the fused AllReduce.  Every output
+    against the oracle run on the device's own input bytes."""
+    import oracle
+    import synthetic_inputs as si
+    w = si.WORKLOADS["n8_bucket25mib_bf16_normal"]
+    n, M = w["n"], w["M"]
+    d = si.generate_device(torch, "bfloat16", w["dist"], n, M, w["seed"], dev,
+                           sigma=w["sigma"])
+    xs = [host_bits(t, "bfloat16") for t in d]
+    q = vc.vc_shard_count(M, n)
+    z = [torch.empty(q, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    y = [torch.empty_like(t) for t in d]
+    timer = CallTimer(torch, dev, stream)
+    b = step_bytes(n, M, 2)
+    chk = Check("full")
+    out = {"config": "N=8, 13,107,200 bf16 normal(0, 1e-3) (one 25 MiB bucket); SUM then AVG, "
+                     "fp32 accumulation; ring; RS-only (ZeRO shards) and fused AR",
+           "q": q, "cases": {}}
+    for op in ("sum", "avg"):
+        rs = vc.prepare_reduce_scatter(d, z, op=op, order="ring")
+        ar = vc.prepare_all_reduce(d, y, op=op, order="ring")
+        t = timer.alternating([("reduce_scatter_only", lambda: rs(stream=stream)),
+                               ("all_reduce", lambda: ar(stream=stream))])
+        torch.cuda.synchronize()
+        oz = oracle.reduce_scatter(xs, "bfloat16", op, "ring")
+        oy = oracle.all_reduce(xs, "bfloat16", op, "ring")
+        for r in range(n):
+            chk.eq("RS", host_bits(z[r], "bfloat16"), oz[r])
+            chk.eq("AR", host_bits(y[r], "bfloat16"), oy[r])
+        out["cases"][op] = {
+            "reduce_scatter_only": call_stats(t["reduce_scatter_only"], b["reduce_scatter"], peak),
+            "all_reduce": call_stats(t["all_reduce"], b["fused_ar"], peak)}
+    out["oracle_check"] = chk.summary()
+    return out
+
+
+def config_c4(torch, vc, dev, stream, peak, workload_name, args, d=None, memory=None):
+    """Four ranks of 67,108,864 elements (fp32 normal(0, 1): 256 MiB per
+    rank; int64 uniform[-2^20, 2^20): 512 MiB): fused AllReduce against
+    ReduceScatter + AllGather against RS-only, alternating, with the peak
+    device memory of each path's buffer lifetime; sampled indices (every
+    chunk boundary included) against the oracle."""
+    import oracle
+    import synthetic_inputs as si
+    w = dict(si.WORKLOADS[workload_name])
+    n, M, dtype = w.pop("n"), w.pop("M"), w.pop("dtype")
+    if d is None:
+        d = si.generate_device(torch, dtype, w.pop("dist"), n, M, w.pop("seed"), dev, **w)
+    es = d[0].element_size()
+    q = vc.vc_shard_count(M, n)
+    y = [torch.empty_like(t) for t in d]
+    sh = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+    y2 = [torch.empty_like(t) for t in d]
+    op, order = "sum", "ring"
+    ar = vc.prepare_all_reduce(d, y, op=op, order=order)
+    dec = vc.prepare_all_reduce_decomposed(d, sh, y2, op=op, order=order)
+    rs = vc.prepare_reduce_scatter(d, sh, op=op, order=order)
+    idx = sample_indices(M, n, q, k=1 << 16)
+    xs_at = sampled_operands(torch, d, idx, dtype)
+    want = oracle.reduce_points(xs_at, idx, n, M, dtype, op, order)
+    timer = CallTimer(torch, dev, stream)
+    t = timer.alternating([("all_reduce", lambda: ar(stream=stream)),
+                           ("rs_then_ag", lambda: dec(stream=stream)),
+                           ("reduce_scatter_only", lambda: rs(stream=stream))])
+    torch.cuda.synchronize()
+    chk = Check("sampled")
+    check_full_sampled(chk, torch, "AR", y, idx, want, dtype)
+    check_full_sampled(chk, torch, "RS+AG", y2, idx, want, dtype)
+    check_rs_sampled(chk, torch, sh, idx, want, n, M, q, dtype, op)
+    b = step_bytes(n, M, es)
+    out = {"config": f"N=4, {M:,} {dtype} per rank ({M * es >> 20} MiB), SUM, ring; fused AR vs "
+                     "RS+AG vs RS-only", "q": q,
+           "paths": {"all_reduce": call_stats(t["all_reduce"], b["fused_ar"], peak),
+                     "rs_then_ag": call_stats(t["rs_then_ag"], b["decomposed_ar"], peak),
+                     "reduce_scatter_only": call_stats(t["reduce_scatter_only"],
+                                                       b["reduce_scatter"], peak)},
+           "oracle_check": chk.summary(indices=int(idx.size))}
+    med = {k: v["median_us"] for k, v in out["paths"].items()}
+    out["rs_then_ag_over_all_reduce"] = (round(med["rs_then_ag"] / med["all_reduce"], 3)
+                                         if out["paths"]["all_reduce"]["stable"]
+                                         and out["paths"]["rs_then_ag"]["stable"] else "unstable")
+    del y, y2, sh, ar, dec, rs
+    torch.cuda.empty_cache()
+    if memory is not None:
+        out["memory_mib"] = memory
+    elif not args.no_memory:
+        out["memory_mib"] = memory_report(torch, vc, d, args, dev)
+    return out
+
+
+def config_c5(torch, vc, dev, stream, peak):
+    """The size x rank-count sweep, summarised: 64 MiB and 1 GiB per rank,
+    N in {2, 4, 8, 16, 64}, int32 / int64 / fp32 / bf16, SUM, ring order.
+    Per point RS, AG and the fused AllReduce (in place) alternate, 3 warm-ups
+    and 10 cycles, each call after an L2-evicting read (at 2 x 64 MiB the
+    data is about the size of the L2, so the previous call's lines would
+    otherwise decide the time); before the timing, a sampled check against
+    the oracle (RS shards, the AllReduce, and the AllGather of the shards)."""
+    import oracle
+    import synthetic_inputs as si
+    timer = CallTimer(torch, dev, stream)
+    rows = []
+    for nbytes in (64 << 20, 1 << 30):
+        for n in (2, 4, 8, 16, 64):
+            for dtype in ("float32", "bfloat16", "int32", "int64"):
+                es = ESIZE[dtype]
+                M = nbytes // es
+                dist = "uniform_pm1" if dtype in ("float32", "bfloat16") else "uniform_int"
+                kw = {} if dist == "uniform_pm1" else {"lo": -100, "hi": 100}
+                d = si.generate_device(torch, dtype, dist, n, M, si.SEED_BASE + 4, dev, **kw)
+                q = vc.vc_shard_count(M, n)
+                z = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+                idx = sample_indices(M, n, q, k=1 << 12, seed=n)
+                xs_at = sampled_operands(torch, d, idx, dtype)
+                rs = vc.prepare_reduce_scatter(d, z, op="sum", order="ring")
+                ar = vc.prepare_all_reduce(d, None, op="sum", order="ring")  # in place
+                ag = vc.prepare_all_gather(z, d)  # writes over the inputs
+                rs(stream=stream)
+                ar(stream=stream)
+                torch.cuda.synchronize()
+                want = oracle.reduce_points(xs_at, idx, n, M, dtype, "sum", "ring")
+                chk = Check("sampled")
+                check_rs_sampled(chk, torch, z, idx, want, n, M, q, dtype, "sum")
+                check_full_sampled(chk, torch, "AR", d, idx, want, dtype)
+                ag(stream=stream)
+                torch.cuda.synchronize()
+                check_full_sampled(chk, torch, "AG", d, idx, want, dtype)
+                t = timer.alternating([("rs", lambda: rs(stream=stream)),
+                                       ("ag", lambda: ag(stream=stream)),
+                                       ("ar", lambda: ar(stream=stream))])
+                b = step_bytes(n, M, es)
+                row = {"n": n, "bytes_per_rank": nbytes, "dtype": dtype}
+                for key, bk in (("rs", "reduce_scatter"), ("ag", "all_gather"), ("ar", "fused_ar")):
+                    st = call_stats(t[key], b[bk], peak)
+                    row[key] = {k: st[k] for k in ("median_us", "p95_us", "cv", "frac")}
+                row["oracle"] = {"indices": int(idx.size), "mismatches": chk.mismatches}
+                rows.append(row)
+                del d, z, rs, ar, ag
+                torch.cuda.empty_cache()
+    fr = [r[k]["frac"] for r in rows for k in ("rs", "ar")]
+    return {"config": "per-rank 64 MiB and 1 GiB x N in {2,4,8,16,64} (N*bytes <= 64 GiB) x "
+                      "int32/int64/fp32/bf16; SUM, ring; RS, AG, fused AR (in place)",
+            "points": rows,
+            "min_frac_rs_ar": round(min(fr), 4),
+            "oracle_mismatches": sum(r["oracle"]["mismatches"] for r in rows)}
+
+
+def configs_report(torch, vc, args, dev, stream, peak, d, memory):
+    """Every configuration the workload list names, each with per-call
+    median / P95 / CV (alternating path order), algorithmic bytes, GB/s, the
+    fraction of the copy peak and its oracle check.  The full-size fp32 four-
+    rank entry reuses the headline's input buffers."""
+    out = {}
+    jobs = (("C1_worked_example_n4_m20_int64", lambda: config_c1(torch, vc, dev, stream, peak)),
+            ("C2_n8_m1000003_f32_uniform", lambda: config_c2(torch, vc, dev, stream, peak)),
+            ("C3_n8_bucket25mib_bf16_normal", lambda: config_c3(torch, vc, dev, stream, peak)),
+            ("C4_n4_256mib_f32_normal",
+             lambda: config_c4(torch, vc, dev, stream, peak, "n4_256mib_f32_normal", args, d,
+                               memory)),
+            ("C4_n4_m67108864_i64_uniform",
+             lambda: config_c4(torch, vc, dev, stream, peak, "n4_m67108864_i64_uniform", args)),
+            ("C5_sweep_summary", lambda: config_c5(torch, vc, dev, stream, peak)))
+    for name, fn in jobs:
+        t0 = time.perf_counter()
+        try:
+            out[name] = fn()
+        except Exception as e:  # recorded in the line, never hidden
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+        out[name]["wall_s"] = round(time.perf_counter() - t0, 1)
+        torch.cuda.empty_cache()
+    return out
 
 
 def transformer_grad_shapes(layers: int = 12, hidden: int = 1024, vocab: int = 32000):
@@ -980,6 +1516,56 @@ def run_sweep(args):
     return 0
 
 
+def run_one(args):
+    """One collective on one synthetic workload, timed back to back: the
+    case a single-kernel profile captures.  --one PATH:DTYPE:N:ELEMENTS,
+    PATH in {rs, ag, ar, dec}; inputs uniform[-1, 1) (floats) or uniform
+    [-100, 100] (integers), seeded; --op / --order as given; W warm-up calls,
+    then K calls between two events.  Prints one JSON line."""
+    import torch
+
+    import allreduce_reducescatter_allgather_gb300 as vc
+    import synthetic_inputs as si
+    path, dtype, n, M = args.one.split(":")
+    n, M = int(n), int(M)
+    if path not in ("rs", "ag", "ar", "dec") or dtype not in ESIZE:
+        raise SystemExit(f"--one {args.one}: PATH in rs/ag/ar/dec, DTYPE in {sorted(ESIZE)}")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    dist = "uniform_pm1" if dtype in ("float32", "bfloat16") else "uniform_int"
+    kw = {} if dist == "uniform_pm1" else {"lo": -100, "hi": 100}
+    d = si.generate_device(torch, dtype, dist, n, M, si.SEED_BASE + 5, dev, **kw)
+    q = vc.vc_shard_count(M, n)
+    z = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+    y = [torch.empty_like(t) for t in d]
+    call = {"rs": lambda: vc.prepare_reduce_scatter(d, z, op=args.op, order=args.order),
+            "ag": lambda: vc.prepare_all_gather(z, y),
+            "ar": lambda: vc.prepare_all_reduce(d, y, op=args.op, order=args.order),
+            "dec": lambda: vc.prepare_all_reduce_decomposed(d, z, y, op=args.op,
+                                                            order=args.order)}[path]()
+    for _ in range(args.warmup):
+        call(stream=stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        call(stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    key = {"rs": "reduce_scatter", "ag": "all_gather", "ar": "fused_ar",
+           "dec": "decomposed_ar"}[path]
+    nbytes = step_bytes(n, M, ESIZE[dtype])[key]
+    peak, kind = measured_peak()
+    g = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"one": args.one, "op": args.op, "order": args.order, "q": q,
+                      "shard_offset_bytes": (q * ESIZE[dtype]) % 16, "calls": args.steps,
+                      "us_per_call": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(g, 1),
+                      "frac": round(g / peak, 4), "peak_kind": kind}), flush=True)
+    return 0
+
+
 def main(argv=None):
     import synthetic_inputs as si
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -1002,6 +1588,11 @@ def main(argv=None):
                     help="run the size x rank-count sweep instead (one JSON line per point)")
     ap.add_argument("--no-memory", action="store_true",
                     help="skip the memory-lifetime, gradient-bucket and latency reports")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration report (every workload, oracle-checked)")
+    ap.add_argument("--one", default="",
+                    help="time one collective instead: PATH:DTYPE:N:ELEMENTS, e.g. "
+                         "rs:bfloat16:12:8388608 (PATH in rs, ag, ar, dec)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -1010,10 +1601,10 @@ def main(argv=None):
         workload["M"] = args.elements
     if args.impl == "reference":
         return run_reference(args, workload)
-    if args.sweep:
+    if args.sweep or args.one:
         import __graft_entry__
         __graft_entry__.build()
-        return run_sweep(args)
+        return run_sweep(args) if args.sweep else run_one(args)
     if dist_info()[0] == 1:
         import __graft_entry__
         __graft_entry__.build()  # under torchrun the library must be built beforehand

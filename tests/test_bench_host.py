@@ -121,3 +121,38 @@ def test_lost_rank_ends_the_collective_with_an_error():
             p.kill()
     assert out[0] == "raised", out
     assert out[1] < 60, out
+
+
+def test_call_stats_marks_unstable_figures():
+    """Median / P95 / CV of per-call times and the median's rate; a ratio is
+    claimable only from figures with CV <= 5 %."""
+    st = bench.call_stats([1.0, 1.0, 1.0, 1.0], 2_000_000, 1000.0)
+    assert st["median_us"] == 1000.0 and st["cv"] == 0.0 and st["stable"]
+    assert st["gbs"] == 2.0 and st["frac"] == 0.002
+    st = bench.call_stats([1.0, 2.0, 1.0, 2.0], 1, 1.0)
+    assert not st["stable"] and st["cv"] > 0.05
+    assert st["p95_us"] == 2000.0
+
+
+def test_sample_indices_cover_every_chunk_boundary():
+    import numpy as np
+    M, n = 1_000_003, 8
+    q = -(-M // n)
+    idx = bench.sample_indices(M, n, q, k=100, seed=3)
+    assert np.all(np.diff(idx) > 0) and idx[0] == 0 and idx[-1] == M - 1
+    for c in range(1, n):
+        assert c * q - 1 in idx and c * q in idx
+
+
+def test_check_counts_mismatches_bitwise():
+    """The comparator works on bits: -0.0 differs from +0.0, NaN equals
+    itself when the payload is the same."""
+    import numpy as np
+    chk = bench.Check("full")
+    a = np.array([1.0, 0.0, np.nan], np.float32)
+    chk.eq("x", a, a.copy())
+    assert chk.mismatches == 0
+    chk.eq("x", np.array([1.0, -0.0, np.nan], np.float32), a)
+    assert chk.mismatches == 1 and chk.compared == 6
+    s = chk.summary(indices=3)
+    assert not s["bit_exact"] and s["indices"] == 3 and s["outputs"] == ["x"]
