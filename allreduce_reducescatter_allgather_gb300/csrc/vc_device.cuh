@@ -926,20 +926,64 @@ __device__ __noinline__ void reduce_one(const ReduceParams& p, long long i) {
     }
 }
 
+// The lanes of a vector that straddles a chunk boundary (or the double
+// tree's halfway point) whose selector is `sel`, stored element by element:
+// lane k holds element i0 + k of chunk c (c + 1 from `cut` on).
+template <class T, int ORDER, bool RS, class A, int V>
+__device__ __forceinline__ void store_lanes(const ReduceParams& p, int c, long long cut,
+                                            long long i0, const Vec<A, V>& acc, int sel) {
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const long long i = i0 + k;
+        const int ci = i >= cut ? c + 1 : c;
+        const int si = (ORDER == kOrderRing) ? ci
+                     : (ORDER == kOrderDoubleTree ? (int)(i >= p.half) : 0);
+        if (si != sel) continue;
+        A r = acc.x[k];
+        if (p.avg) r = avg_div(r, p.n);
+        if constexpr (RS) {
+            store1(static_cast<T*>(p.out[ci]) + (i - (long long)ci * p.q), r);
+        } else {
+            for (int s = 0; s < p.nout; ++s) store1(static_cast<T*>(p.out[s]) + i, r);
+        }
+    }
+}
+
 // One vector slot on its own, in the kernels with a compile-time N: the
 // vector path if it lies inside one chunk and inside the data on aligned
-// bases, else element by element.
+// bases; inside the data but across a chunk boundary or the double tree's
+// halfway point, the N operand vectors load whole and the fold runs once
+// per selector among the lanes (each lane keeps its own); else (misaligned
+// bases, the end of the data, the padding, shards shorter than a vector)
+// element by element.  Element by element, a straddling vector's thread
+// waited for one round of loads per element and finished microseconds
+// after the rest of the grid (fp32 ReduceScatter, 8 ranks x 1,000,003:
+// 8.0 us per call against 6.1 us with M = 1,000,000).  The kernel calls this
+// only from whole warps (see reduce_body).
 template <class T, class Op, int ORDER, int NT, bool RS>
 __device__ __noinline__ void reduce_slot(const ReduceParams& p, long long v) {
     constexpr int V = Traits<T>::V;
     const long long i0 = v * V;
     const int c = chunk_of(i0, p.q, p.inv_q, p.n);
-    const bool one_tree = (ORDER != kOrderDoubleTree) || i0 >= p.half || i0 + V <= p.half;
-    if (p.vec_ok && one_tree && i0 + V <= p.M && i0 + V <= (long long)(c + 1) * p.q) {
+    const long long cut = (long long)(c + 1) * p.q;  // lanes from here are in chunk c + 1
+    const bool one_chunk = i0 + V <= cut;
+    if (p.vec_ok && i0 + V <= p.M && (one_chunk || p.q >= V)) {
+        const int s0 = (ORDER == kOrderRing) ? c
+                     : (ORDER == kOrderDoubleTree ? (int)(i0 >= p.half) : 0);
+        const long long last = i0 + V - 1;
+        const int s1 = (ORDER == kOrderRing) ? (one_chunk ? c : c + 1)
+                     : (ORDER == kOrderDoubleTree ? (int)(last >= p.half) : 0);
         VecLoader<T> ld{p, i0};
-        const int sel = (ORDER == kOrderDoubleTree) ? (i0 >= p.half) : c;
-        auto acc = fold<Op, ORDER, NT>(ld, p.n, sel);
-        store_result<T, NT, RS>(p, c, i0, acc, false);
+        auto acc = fold<Op, ORDER, NT>(ld, p.n, s0);
+        if (one_chunk && s0 == s1) {
+            store_result<T, NT, RS>(p, c, i0, acc, false);
+            return;
+        }
+        store_lanes<T, ORDER, RS>(p, c, cut, i0, acc, s0);
+        if (s1 != s0) {
+            acc = fold<Op, ORDER, NT>(ld, p.n, s1);
+            store_lanes<T, ORDER, RS>(p, c, cut, i0, acc, s1);
+        }
     } else {
         for (int k = 0; k < V && i0 + k < p.limit; ++k) reduce_one<T, Op, ORDER, NT, RS>(p, i0 + k);
     }
@@ -1098,6 +1142,13 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
             const int c_lane0 = __shfl_sync(kFullWarp, c, 0);
             warp_shard = __all_sync(kFullWarp, wide && c == c_lane0);
         }
+        // With a compile-time N, a warp with any lane off the vector path
+        // sends every lane through reduce_slot, an out-of-line function, so
+        // that it is never called from part of a warp while the rest of the
+        // warp runs the vector path (a divergent call of that kind gave the
+        // other lanes wrong results in the run-time-N kernels, which now
+        // inline their slot path instead).  Every lane reaches this point.
+        if constexpr (NT > 0) wide = __all_sync(kFullWarp, wide);
         if (wide) {
             if constexpr (kPre) {
                 uint4 buf[NT][U];
