@@ -1576,7 +1576,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="n4_256mib_f32_normal", choices=sorted(si.WORKLOADS))
     ap.add_argument("--op", default="sum", choices=["sum", "prod", "max", "min", "avg"])
     ap.add_argument("--order", default="ring",
-                    choices=["ring", "recursive_halving", "pairwise_tree"])
+                    choices=["ring", "recursive_halving", "pairwise_tree",
+                             "double_binary_tree"])
     ap.add_argument("--elements", type=int, default=0,
                     help="override the elements per rank (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=20)
