@@ -1244,12 +1244,50 @@ def config_c5(torch, vc, dev, stream, peak):
                 rows.append(row)
                 del d, z, rs, ar, ag
                 torch.cuda.empty_cache()
+    # every op and order at one point: eight ranks, 64 MiB per rank, the
+    # float types (the integer types give the same bits in every order)
+    combos = []
+    n, nbytes = 8, 64 << 20
+    for dtype in ("float32", "bfloat16"):
+        M = nbytes // ESIZE[dtype]
+        d = si.generate_device(torch, dtype, "uniform_pm1", n, M, si.SEED_BASE + 6, dev)
+        q = vc.vc_shard_count(M, n)
+        z = [torch.empty(q, dtype=d[0].dtype, device=dev) for _ in range(n)]
+        y = [torch.empty_like(t) for t in d]
+        idx = sample_indices(M, n, q, k=1 << 12, seed=8)
+        xs_at = sampled_operands(torch, d, idx, dtype)
+        b = step_bytes(n, M, ESIZE[dtype])
+        for order in ("ring", "recursive_halving", "pairwise_tree", "double_binary_tree"):
+            for op in ("sum", "max", "min", "prod"):
+                rs = vc.prepare_reduce_scatter(d, z, op=op, order=order)
+                ar = vc.prepare_all_reduce(d, y, op=op, order=order)
+                rs(stream=stream)
+                ar(stream=stream)
+                torch.cuda.synchronize()
+                want = oracle.reduce_points(xs_at, idx, n, M, dtype, op, order)
+                chk = Check("sampled")
+                check_rs_sampled(chk, torch, z, idx, want, n, M, q, dtype, op)
+                check_full_sampled(chk, torch, "AR", y, idx, want, dtype)
+                t = timer.alternating([("rs", lambda: rs(stream=stream)),
+                                       ("ar", lambda: ar(stream=stream))])
+                row = {"dtype": dtype, "order": order, "op": op}
+                for key, bk in (("rs", "reduce_scatter"), ("ar", "fused_ar")):
+                    st = call_stats(t[key], b[bk], peak)
+                    row[key] = {k: st[k] for k in ("median_us", "cv", "frac")}
+                row["oracle"] = {"indices": int(idx.size), "mismatches": chk.mismatches}
+                combos.append(row)
+        del d, z, y, rs, ar
+        torch.cuda.empty_cache()
     fr = [r[k]["frac"] for r in rows for k in ("rs", "ar")]
+    fo = [r[k]["frac"] for r in combos for k in ("rs", "ar")]
     return {"config": "per-rank 64 MiB and 1 GiB x N in {2,4,8,16,64} (N*bytes <= 64 GiB) x "
-                      "int32/int64/fp32/bf16; SUM, ring; RS, AG, fused AR (in place)",
+                      "int32/int64/fp32/bf16; SUM, ring; RS, AG, fused AR (in place); and at "
+                      "8 ranks x 64 MiB, fp32/bf16, every op x order, RS and AR",
             "points": rows,
             "min_frac_rs_ar": round(min(fr), 4),
-            "oracle_mismatches": sum(r["oracle"]["mismatches"] for r in rows)}
+            "ops_orders_n8_64mib": combos,
+            "ops_orders_min_frac_rs_ar": round(min(fo), 4),
+            "oracle_mismatches": sum(r["oracle"]["mismatches"] for r in rows + combos)}
 
 
 def configs_report(torch, vc, args, dev, stream, peak, d, memory):
