@@ -541,6 +541,29 @@ def test_in_place(env, dtype):
             assert_bits_equal(to_host(d2[r], dtype), oy[r], dtype, f"in-place dec {order}")
 
 
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+def test_in_place_straddling_vectors(env, dtype):
+    """In-place AllReduce where vectors straddle chunk boundaries (and the
+    double tree's halfway point): the straddling path folds the vector once
+    per chunk and stores each fold's lanes element by element, so the second
+    fold re-reads a vector whose other lanes the first fold already
+    overwrote.  Run-time N (12, 33) and compile-time N (6, 8), every order,
+    SUM and AVG, against the oracle."""
+    vc, torch = env.vc, env.torch
+    for n in (6, 8, 12, 33):
+        M = 7 * n * 1024 + 5 * n + 3  # q = 7174: not a whole number of vectors
+        for order in orders_for(n):
+            for op in ("sum", "avg") if dtype != "int32" else ("sum", "max"):
+                xs = gen(dtype, n, M, seed=n * 131 + len(order))
+                oy = oracle.all_reduce(xs, dtype, op, order)
+                d = to_device(torch, xs, dtype, env.dev)
+                vc.vc_all_reduce(d, None, op=op, order=order)
+                torch.cuda.synchronize()
+                for r in range(n):
+                    assert_bits_equal(to_host(d[r], dtype), oy[r], dtype,
+                                      f"in-place N={n} {order} {op} rank {r}")
+
+
 ESIZE = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}
 
 
