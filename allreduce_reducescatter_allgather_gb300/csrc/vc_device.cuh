@@ -130,10 +130,15 @@ __device__ __forceinline__ uint4 pack(const Vec<float, 4>& a, float*) {
 __device__ __forceinline__ unsigned bf16_bits(float f) {
     return (unsigned)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// Two lanes per conversion (each rounded to nearest even on its own, lane
+// 2k in the low half): the bits of two bf16_bits calls, in one instruction.
 __device__ __forceinline__ uint4 pack(const Vec<float, 8>& a, __nv_bfloat16*) {
     unsigned w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = bf16_bits(a.x[2 * k]) | (bf16_bits(a.x[2 * k + 1]) << 16);
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a.x[2 * k], a.x[2 * k + 1]);
+        w[k] = *reinterpret_cast<const unsigned*>(&h);
+    }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -364,16 +369,42 @@ __device__ __forceinline__ uint4 ld_warp_realigned(const void* src) {
 // a (+) b with the running value on the left.  Floats: one IEEE single
 // operation, explicitly rounded (no contraction into FMA).  Integers: wrap
 // modulo 2^64.  MAX/MIN keep a on ties.
+// Two float lanes in one 64-bit register (lane 0 in the low half), for the
+// paired single-precision instructions: each lane is one IEEE single
+// operation rounded to nearest even, as __fadd_rn / __fmul_rn give, in half
+// the instructions.
+__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
+    return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f32x2_lo(unsigned long long v) { return __uint_as_float((unsigned)v); }
+__device__ __forceinline__ float f32x2_hi(unsigned long long v) {
+    return __uint_as_float((unsigned)(v >> 32));
+}
+
 struct OpSum {
+    static constexpr bool kPaired = true;
     __device__ static __forceinline__ float apply(float a, float b) { return __fadd_rn(a, b); }
     __device__ static __forceinline__ long long apply(long long a, long long b) {
         return (long long)((unsigned long long)a + (unsigned long long)b);
     }
+    __device__ static __forceinline__ unsigned long long apply2(unsigned long long a,
+                                                               unsigned long long b) {
+        unsigned long long r;
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+        return r;
+    }
 };
 struct OpProd {
+    static constexpr bool kPaired = true;
     __device__ static __forceinline__ float apply(float a, float b) { return __fmul_rn(a, b); }
     __device__ static __forceinline__ long long apply(long long a, long long b) {
         return (long long)((unsigned long long)a * (unsigned long long)b);
+    }
+    __device__ static __forceinline__ unsigned long long apply2(unsigned long long a,
+                                                               unsigned long long b) {
+        unsigned long long r;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+        return r;
     }
 };
 struct OpMax {
@@ -420,11 +451,25 @@ template <> struct Identity<__nv_bfloat16, OpMin> {
     __device__ static __forceinline__ float get() { return IdentityF<float>::pos_inf(); }
 };
 
+// Whether Op has the paired float form (sum and product; max and min do not).
+template <class Op, class = void> struct HasPaired : std::false_type {};
+template <class Op> struct HasPaired<Op, std::void_t<decltype(Op::kPaired)>> : std::true_type {};
+
 template <class Op, class A, int W>
 __device__ __forceinline__ Vec<A, W> vop(const Vec<A, W>& a, const Vec<A, W>& b) {
     Vec<A, W> r;
+    if constexpr (std::is_same<A, float>::value && W % 2 == 0 && HasPaired<Op>::value) {
 #pragma unroll
-    for (int k = 0; k < W; ++k) r.x[k] = Op::apply(a.x[k], b.x[k]);
+        for (int k = 0; k < W; k += 2) {
+            const unsigned long long v =
+                Op::apply2(f32x2(a.x[k], a.x[k + 1]), f32x2(b.x[k], b.x[k + 1]));
+            r.x[k] = f32x2_lo(v);
+            r.x[k + 1] = f32x2_hi(v);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < W; ++k) r.x[k] = Op::apply(a.x[k], b.x[k]);
+    }
     return r;
 }
 
