@@ -190,9 +190,15 @@ def test_bucketed_equals_per_tensor_for_chunk_free_orders(genv):
                 grads[r][t].copy_(src[r][t])
         gb.all_reduce_tensors(order=order)
         for t in range(len(SHAPES)):
+            # the oracle's AllReduce of the tensor on its own, wherever the
+            # bucket put it, and the library's per-tensor call
+            xs = [to_host(src[r][t].reshape(-1), "float32") for r in range(n)]
+            want = oracle.all_reduce(xs, "float32", "sum", order)
             ref = [torch.empty_like(src[0][t]) for _ in range(n)]
             vc.vc_all_reduce([src[r][t] for r in range(n)], ref, order=order)
             for r in range(n):
+                assert_bits_equal(to_host(grads[r][t].reshape(-1), "float32"), want[r],
+                                  "float32", f"bucketed {order} tensor {t} rank {r}")
                 assert torch.equal(grads[r][t], ref[r])
 
 
@@ -298,9 +304,13 @@ def test_fused_bucket_in_place_equals_bucket_views(genv):
     gb.all_reduce(op="sum", order="ring")
     gb.all_reduce_tensors(op="sum", order="ring", fused=True)
     torch.cuda.synchronize()
+    host = [[to_host(g.reshape(-1), "bfloat16") for g in row] for row in src]
+    want = _oracle_buckets(gb, host, "bfloat16", "sum", "ring")
     for r in range(n):
         for t, v in enumerate(gb.views(r)):
             assert torch.equal(grads[r][t], v)
+            assert_bits_equal(to_host(grads[r][t].reshape(-1), "bfloat16"), want[r][t],
+                              "bfloat16", f"fused in place tensor {t} rank {r}")
 
 
 @pytest.mark.gpu
@@ -329,6 +339,10 @@ def test_fused_buckets_replay_from_a_cuda_graph(genv):
         g.replay()
         gb.all_reduce(op="sum", order="ring")
         torch.cuda.synchronize()
+        host = [[to_host(x.reshape(-1), "float32") for x in row] for row in src]
+        want = _oracle_buckets(gb, host, "float32", "sum", "ring")
         for r in range(n):
             for t, v in enumerate(gb.views(r)):
                 assert torch.equal(grads[r][t], v), (it, r, t)
+                assert_bits_equal(to_host(grads[r][t].reshape(-1), "float32"), want[r][t],
+                                  "float32", f"replay {it} tensor {t} rank {r}")
