@@ -366,9 +366,6 @@ __device__ __forceinline__ uint4 ld_warp_realigned(const void* src) {
 
 // ------------------------------------------------------------------- ops --
 
-// a (+) b with the running value on the left.  Floats: one IEEE single
-// operation, explicitly rounded (no contraction into FMA).  Integers: wrap
-// modulo 2^64.  MAX/MIN keep a on ties.
 // Two float lanes in one 64-bit register (lane 0 in the low half), for the
 // paired single-precision instructions: each lane is one IEEE single
 // operation rounded to nearest even, as __fadd_rn / __fmul_rn give, in half
@@ -381,6 +378,10 @@ __device__ __forceinline__ float f32x2_hi(unsigned long long v) {
     return __uint_as_float((unsigned)(v >> 32));
 }
 
+// a (+) b with the running value on the left.  Floats: one IEEE single
+// operation, explicitly rounded (no contraction into FMA); SUM and PROD also
+// have the paired form apply2.  Integers: wrap modulo 2^64.  MAX/MIN keep a
+// on ties.
 struct OpSum {
     static constexpr bool kPaired = true;
     __device__ static __forceinline__ float apply(float a, float b) { return __fadd_rn(a, b); }
