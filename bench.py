@@ -496,7 +496,6 @@ def run_ours(args, workload: dict):
     buckets = bucket_report(torch, vc, args, dev) if not args.no_memory else None
     latency = latency_table(torch, vc, args, dev, peak) if not args.no_memory else None
     e2e = e2e_measure(torch, vc, d, args, dev, stream, by["step"])
-    read_peak = read_probe(torch, dev, peak)
     configs = (configs_report(torch, vc, args, dev, stream, peak, d, memory)
                if (world == 1 and not args.no_configs
                    and M == si.WORKLOADS[args.workload]["M"]) else None)
@@ -511,7 +510,6 @@ def run_ours(args, workload: dict):
         "paths": paths,
         "gpu_launches": 3 * args.steps,
         "e2e": e2e,
-        "read_only_stream": read_peak,
     }
     if clk is not None:
         line["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
@@ -549,27 +547,6 @@ def run_ours(args, workload: dict):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
-
-
-def read_probe(torch, dev, peak: float, nbytes: int = 2 << 30, reps: int = 5) -> dict:
-    """Context for the read-dominated ReduceScatter, whose rate can exceed
-    the copy peak: a read-only stream in this run (torch's sum over 2 GiB of
-    fp32, best of `reps`, CUDA events), in GB/s and against the copy peak."""
-    x = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
-    out = torch.empty((), dtype=torch.float32, device=dev)
-    torch.sum(x, dim=0, out=out)
-    best = 0.0
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        torch.sum(x, dim=0, out=out)
-        b.record()
-        b.synchronize()
-        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
-    del x
-    torch.cuda.empty_cache()
-    return {"gbs": round(best, 1), "frac_of_copy_peak": round(best / peak, 4),
-            "how": f"torch.sum over {nbytes >> 30} GiB of fp32, best of {reps}"}
 
 
 def link_probe(torch, dev, nbytes: int = 1 << 30, reps: int = 3) -> dict:
