@@ -1270,15 +1270,23 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
 // operands at a time): two, so that a second block hides the first one's
 // load latency; measured, the ring at N = 12 went from 0.81x to 0.96x (bf16
 // 0.67x to 0.82x).
-template <int NT>
+//
+// One exception: the bf16 ReduceScatter at N = 4 .. 8 asks for three blocks.
+// At N = 4 and 8 its fold takes 87-88 registers under the one-block bound,
+// just over the 85 that fit three blocks; bound to three it takes 76 with no
+// spills.  The ReduceScatter, which reads N streams per store, gains from
+// the extra warps' loads in flight: measured 0.5-1.5 points of the copy peak
+// (N = 8 1.046x -> 1.052x, the 25 MiB bucket on 8 ranks 0.982x -> 0.993x);
+// the AllReduce and the fp32 ReduceScatter gained nothing.
+template <int NT, bool RS = false, int ES = 4>
 constexpr int min_blocks() {
-    return NT > 0 ? 1 : 2;
+    return NT > 0 ? ((RS && ES == 2 && NT >= 4 && NT <= 8) ? 3 : 1) : 2;
 }
 
 // ReduceScatter: index space [0, N*q), one store per element into the shard
 // that owns it.
 template <class T, class Op, int ORDER, int NT, int U>
-__global__ void __launch_bounds__(kThreads, min_blocks<NT>()) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kThreads, min_blocks<NT, true, sizeof(T)>()) vc_rs_kernel(const __grid_constant__ ReduceParams p) {
     reduce_body<T, Op, ORDER, NT, U, true>(p);
 }
 
