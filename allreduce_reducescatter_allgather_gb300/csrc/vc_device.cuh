@@ -456,10 +456,15 @@ template <> struct Identity<__nv_bfloat16, OpMin> {
 template <class Op, class = void> struct HasPaired : std::false_type {};
 template <class Op> struct HasPaired<Op, std::void_t<decltype(Op::kPaired)>> : std::true_type {};
 
+// The paired form serves the eight fp32 lanes of a bf16 vector only.  For
+// fp32's four lanes it measured no gain, and building the register pairs
+// pushed the fp32 trees with a run-time N over 128 registers into spills
+// (fp32 ReduceScatter, tree order, 12 ranks: 1.02x -> 0.68x of the copy
+// peak).
 template <class Op, class A, int W>
 __device__ __forceinline__ Vec<A, W> vop(const Vec<A, W>& a, const Vec<A, W>& b) {
     Vec<A, W> r;
-    if constexpr (std::is_same<A, float>::value && W % 2 == 0 && HasPaired<Op>::value) {
+    if constexpr (std::is_same<A, float>::value && W == 8 && HasPaired<Op>::value) {
 #pragma unroll
         for (int k = 0; k < W; k += 2) {
             const unsigned long long v =
@@ -787,13 +792,18 @@ __device__ __forceinline__ VecOf<Ld> fold_tree(const Ld& ld) {
 // compile-time constant every test folds away; with a run-time n they are
 // uniform branches.
 
-// t[K] holds rank BASE + K (absent ranks are never read).
+// t[K] holds rank BASE + K (absent ranks are never read).  A subtree whose
+// ranks all exist (its last rank P + L - 1 below n) takes the unchecked
+// evaluation: with a run-time n the checks otherwise cost every node of
+// every vector a compare and a branch (bf16 ReduceScatter over 12 ranks in
+// the tree order ran 26 % more instructions than the ring).
 template <class Op, int K, int L, class Ld, class R, int G>
 __device__ __forceinline__ VecOf<Ld> tree_local_n(const Ld& ld, const R (&t)[G], int base, int n) {
     if constexpr (L == 1) {
         return ld.cvt(t[K]);
     } else {
         const int P = base + K;
+        if (P + L - 1 < n) return tree_local<Op, K, L>(ld, t);
         VecOf<Ld> l = tree_local_n<Op, K - L / 2, L / 2>(ld, t, base, n);
         if (P >= n) return l;
         if (P + 1 >= n) return vop<Op>(l, ld.cvt(t[K]));
