@@ -118,44 +118,45 @@ __device__ __forceinline__ void bucket_fill(const BucketParams& p, long long lo,
 
 // NT > 0: N known at compile time; a thread loads the N x U operand vectors
 // of its U vectors (blockDim.x apart) into registers before folding any, as
-// the AllReduce kernel does.  NT == 0: a run-time N, one vector at a time.
+// the AllReduce kernel does; the slots of a span past the tile's last vector
+// load and store nothing.  NT == 0: a run-time N, one vector at a time.
 // The tiles come in bucket order (vc_bucket_plan writes them so); for the
 // ReduceScatter, the block of tile t also fills the uncovered positions up
 // to the next tile (tile 0's block, those before it too).
+//
+// Resident blocks: bf16 with N = 4 .. 8 asks for three (at most 80
+// registers), everything else for two.  Measured on GB300 (a 24 MiB bucket
+// of bf16 tensors on 8 ranks, ncu): at two blocks the ReduceScatter ran
+// 19 % behind the ReduceScatter of the packed bucket, with the same DRAM
+// bytes and two thirds of its warps.  The compile-time path then also
+// handles a tile's partial last span itself (predicated loads) instead of
+// the run-time-N vector fold, whose 16-operand groups set the kernel's
+// register count (116 -> 76-80).  Each block sets up its tile (descriptor,
+// then the N pointers into shared memory) before loading any operand; with
+// three blocks per SM that latency overlaps the other blocks' streams, and
+// prefetching the next tile's set-up measured no faster.  The bucket
+// ReduceScatter of 351 MiB of bf16 tensors on 8 ranks: 559 -> 524 us (the
+// packed bucket: 497 us); the AllReduce 921 -> 915 us (878 us).
 template <class T, class Op, int NT, int U, bool RS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, (sizeof(T) == 2 && NT >= 4 && NT <= 8) ? 3 : 2)
     vc_bucket_kernel(const __grid_constant__ BucketParams p) {
     constexpr int V = Traits<T>::V;
     __shared__ const void* s_in[2 * kMaxRanks];
     __shared__ void* s_out[RS ? 1 : kMaxRanks];
-    // Software-pipelined tile set-up: while a block works on tile t it has
-    // already fetched tile t + gridDim.x's descriptor and (threads r < N)
-    // that tile's pointers, so a new tile starts after one shared-memory
-    // round trip instead of a chain of dependent global loads.
     // launched with programmatic stream serialization: wait for the kernel
     // before this one to complete (and its writes to be visible) first
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    int t = blockIdx.x;
-    if (t >= p.ntiles) return;
-    vc_bucket_tile_t tile = p.tiles[t];
     const int me = threadIdx.x;  // < kThreads; threads below n carry pointers
-    const void* my_in = me < p.n ? p.in[(long long)tile.tensor * p.n + me] : nullptr;
-    void* my_out = nullptr;
-    if constexpr (!RS) my_out = me < p.n ? p.out[(long long)tile.tensor * p.n + me] : nullptr;
-    for (; t < p.ntiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const vc_bucket_tile_t tile = p.tiles[t];
         __syncthreads();  // the last tile's readers are done with the tables
         if (me < p.n) {
-            s_in[me] = my_in;
-            s_in[me + p.n] = my_in;
-            if constexpr (!RS) s_out[me] = my_out;
+            const void* a = p.in[(long long)tile.tensor * p.n + me];
+            s_in[me] = a;
+            s_in[me + p.n] = a;
+            if constexpr (!RS) s_out[me] = p.out[(long long)tile.tensor * p.n + me];
         }
         __syncthreads();
-        const int tn = t + gridDim.x;
-        vc_bucket_tile_t next_tile = tile;
-        if (tn < p.ntiles) next_tile = p.tiles[tn];
-        long long next_start = 0;  // ReduceScatter: where the next tile starts
-        if constexpr (RS)
-            next_start = t + 1 < p.ntiles ? p.tiles[t + 1].bucket_offset : (long long)p.n * p.q;
         const bool valid = tile_in_plan(tile, p);  // the same in every thread
         const int c = valid ? (int)(tile.bucket_offset / p.q) : 0;  // the tile's ring chunk
         const long long nvec = (valid && (tile.flags & 1)) ? tile.count / V : 0;
@@ -163,31 +164,34 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (long long b0 = 0; b0 < nvec; b0 += span) {
             const long long v0 = b0 + threadIdx.x;
             if constexpr (NT > 0) {
-                if (v0 + (long long)(U - 1) * blockDim.x < nvec) {
-                    uint4 buf[NT][U];
+                uint4 buf[NT][U];
 #pragma unroll
-                    for (int r = 0; r < NT; ++r) {
-                        const T* base = static_cast<const T*>(s_in[r]) + tile.tensor_offset + v0 * V;
+                for (int r = 0; r < NT; ++r) {
+                    const T* base = static_cast<const T*>(s_in[r]) + tile.tensor_offset + v0 * V;
 #pragma unroll
-                        for (int u = 0; u < U; ++u) buf[r][u] = ld16(base + (long long)u * blockDim.x * V);
-                    }
+                    for (int u = 0; u < U; ++u)
+                        buf[r][u] = v0 + (long long)u * blockDim.x < nvec
+                                        ? ld16(base + (long long)u * blockDim.x * V)
+                                        : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
+                for (int u = 0; u < U; ++u) {
+                    if (v0 + (long long)u * blockDim.x < nvec) {
                         PreLoader<T, NT, U> ld{buf, u};
                         auto acc = fold<Op, kOrderRing, NT>(ld, NT, c);
                         const long long j = (v0 + (long long)u * blockDim.x) * V;
                         bucket_store<T, RS>(p, s_out, c, tile.tensor_offset + j,
                                             tile.bucket_offset + j, acc);
                     }
-                    continue;
                 }
-            }
+            } else {
 #pragma unroll 1
-            for (int u = 0; u < U; ++u) {
-                const long long v = v0 + (long long)u * blockDim.x;
-                if (v < nvec)
-                    bucket_vector<T, Op, RS>(p, s_in, s_out, c, tile.tensor_offset + v * V,
-                                             tile.bucket_offset + v * V);
+                for (int u = 0; u < U; ++u) {
+                    const long long v = v0 + (long long)u * blockDim.x;
+                    if (v < nvec)
+                        bucket_vector<T, Op, RS>(p, s_in, s_out, c, tile.tensor_offset + v * V,
+                                                 tile.bucket_offset + v * V);
+                }
             }
         }
         // the tile's tail, or all of it when its addresses are not aligned
@@ -197,15 +201,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                                       tile.bucket_offset + j);
         if constexpr (RS) {
             if (valid) {
+                const long long next_start =
+                    t + 1 < p.ntiles ? p.tiles[t + 1].bucket_offset : (long long)p.n * p.q;
                 if (t == 0) bucket_fill<T, Op>(p, 0, tile.bucket_offset);
                 bucket_fill<T, Op>(p, tile.bucket_offset + tile.count, next_start);
-            }
-        }
-        if (tn < p.ntiles) {
-            tile = next_tile;
-            if (me < p.n) {
-                my_in = p.in[(long long)tile.tensor * p.n + me];
-                if constexpr (!RS) my_out = p.out[(long long)tile.tensor * p.n + me];
             }
         }
     }
@@ -217,7 +216,11 @@ template <class T, class Op, int NT, int U>
 cudaError_t launch_bucket_n(const BucketParams& p, bool rs, cudaStream_t st) {
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
-    const int blocks = std::min(p.ntiles, 16 * sms);
+    // one block per tile up to 64 per SM, as the reduction kernels size
+    // their grids (with 8 KiB tiles a 25 MiB bucket is ~3,200 tiles; capped
+    // at 16 per SM, the bucket AllReduce of 351 MiB of bf16 tensors on 8
+    // ranks measured 902 us against 897 us)
+    const int blocks = std::min(p.ntiles, 64 * sms);
     if (rs) return launch_pdl(vc_bucket_kernel<T, Op, NT, U, true>, dim3(blocks), dim3(kThreads), st, p);
     return launch_pdl(vc_bucket_kernel<T, Op, NT, U, false>, dim3(blocks), dim3(kThreads), st, p);
 }

@@ -256,9 +256,10 @@ typedef struct {
 
 /* The largest tile vc_bucket_plan makes, per rank.  (Measured on GB300 with
  * a 351 MiB set of 145 bf16 tensors on 8 ranks: 64 KiB tiles ran 13 % behind
- * the in-bucket AllReduce, 16 KiB tiles 4 %: more, smaller tiles balance the
- * last wave of blocks.) */
-#define VC_BUCKET_TILE_MAX_BYTES (1u << 14)
+ * the in-bucket AllReduce, 16 KiB tiles 4 %, 8 KiB tiles 2 %: more, smaller
+ * tiles balance the last wave of blocks.  The bucket AllGather lost 1 % from
+ * 16 to 8 KiB, the ReduceScatter did not move.) */
+#define VC_BUCKET_TILE_MAX_BYTES (1u << 13)
 
 /* Plans a fused bucket AllReduce (host only; launches nothing).
  * sendbufs, recvbufs: HOST arrays of ntensors * nranks DEVICE pointers,

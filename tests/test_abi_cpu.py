@@ -421,7 +421,7 @@ def test_bucket_plan_tiles_partition_the_tensors(vc, seed):
     """Tiles cover every element of every tensor exactly once, in order;
     each sits at the tensor's bucket offset plus its tensor offset; none
     crosses a ring chunk (a multiple of ceil(bucket_count / N)); none is
-    larger than 16 KiB; flags bit 0 is set exactly when every rank's input
+    larger than 8 KiB; flags bit 0 is set exactly when every rank's input
     and output address of the tile start is 16-byte aligned."""
     import random
     rng = random.Random(seed)
@@ -441,7 +441,7 @@ def test_bucket_plan_tiles_partition_the_tensors(vc, seed):
     q = -(-total // n) if total else 1
     seen = {k: 0 for k in range(len(counts))}
     for t in tiles:
-        assert t.count > 0 and t.count * es <= 16 << 10   # VC_BUCKET_TILE_MAX_BYTES
+        assert t.count > 0 and t.count * es <= 8 << 10   # VC_BUCKET_TILE_MAX_BYTES
         assert t.tensor_offset == seen[t.tensor], "tiles of a tensor follow each other"
         seen[t.tensor] += t.count
         assert t.bucket_offset == base[t.tensor] + t.tensor_offset
