@@ -625,15 +625,22 @@ def e2e_measure(torch, vc, d, args, dev, stream, step_bytes_):
               vc.prepare_all_reduce_decomposed(di, dsh, dy2, op=args.op, order=args.order))
              for _, di, dy, dsh, dy2 in sets]
 
-    def run(steps):
+    phases = []  # per timed step: events around its host-to-device and device-to-host copies
+
+    def run(steps, timed=False):
         for k in range(steps):
             j = k % 2
             flat = sets[j][0]
             hy, hy2 = host_out[j]
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
             if k >= 2:
                 s_in.wait_event(comp_done[j])  # set j's inputs no longer read
             with torch.cuda.stream(s_in):
+                if marks:
+                    marks[0].record(s_in)
                 flat[0].copy_(host_in, non_blocking=True)
+                if marks:
+                    marks[1].record(s_in)
             in_ready[j].record(s_in)
             stream.wait_event(in_ready[j])
             if k >= 2:
@@ -644,9 +651,15 @@ def e2e_measure(torch, vc, d, args, dev, stream, step_bytes_):
             comp_done[j].record(stream)
             s_out.wait_event(comp_done[j])
             with torch.cuda.stream(s_out):
+                if marks:
+                    marks[2].record(s_out)
                 hy.copy_(flat[1], non_blocking=True)
                 hy2.copy_(flat[2], non_blocking=True)
+                if marks:
+                    marks[3].record(s_out)
             out_done[j].record(s_out)
+            if marks:
+                phases.append(marks)
 
     run(2)
     torch.cuda.synchronize()
@@ -654,7 +667,7 @@ def e2e_measure(torch, vc, d, args, dev, stream, step_bytes_):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(s_in)
-    run(args.e2e_steps)
+    run(args.e2e_steps, timed=True)
     s_in.wait_stream(s_out)
     s_in.wait_stream(stream)
     b.record(s_in)
@@ -672,6 +685,19 @@ def e2e_measure(torch, vc, d, args, dev, stream, step_bytes_):
     link["e2e_frac_of_both"] = round(host_gbs / link["both_gbs"], 4) if link["both_gbs"] else None
     serial_ms = (h2d / link["h2d_gbs"] + d2h / link["d2h_gbs"]) / 1e6
     link["serial_link_ms_per_step"] = round(serial_ms, 3)
+    # where the step's time goes: each direction's copy time per step (its
+    # events on its own stream) and the share of the step the device-to-host
+    # stream spent copying (1.0: the outbound link never waited for compute)
+    h2d_ms = sum(m[0].elapsed_time(m[1]) for m in phases) / len(phases)
+    d2h_ms = sum(m[2].elapsed_time(m[3]) for m in phases) / len(phases)
+    link["h2d_ms_per_step"] = round(h2d_ms, 3)
+    link["d2h_ms_per_step"] = round(d2h_ms, 3)
+    link["d2h_busy_frac"] = round(d2h_ms / ms, 4)
+    # the rates the copies reached inside the step, against the probe's
+    # best-of-3 above: the host link is shared with whatever else runs on
+    # the host, and the step gets what is left of it
+    link["h2d_gbs_in_step"] = round(h2d / (h2d_ms / 1e3) / 1e9, 1)
+    link["d2h_gbs_in_step"] = round(d2h / (d2h_ms / 1e3) / 1e9, 1)
     return {"value": round(step_bytes_ / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "host_wall_ms_per_step": round(wall_ms, 3), "steps": args.e2e_steps,
