@@ -820,10 +820,10 @@ def latency_table(torch, vc, args, dev, peak, K: int = 16):
                  "decomposed": call_stats([v / scale for v in t["decomposed"]],
                                           b["decomposed_ar"], peak)}
             for mode in ("direct", "decomposed"):
-                r[mode]["payload_gbs"] = round(nbytes * n / r[mode]["median_us"] / 1e3, 2)
+                r[mode]["payload_gbs"] = round(nbytes * n / r[mode]["mean_us"] / 1e3, 2)
             stable = r["direct"]["stable"] and r["decomposed"]["stable"]
-            r["decomposed_over_direct"] = (round(r["decomposed"]["median_us"]
-                                                 / r["direct"]["median_us"], 3)
+            r["decomposed_over_direct"] = (round(r["decomposed"]["mean_us"]
+                                                 / r["direct"]["mean_us"], 3)
                                            if stable else "unstable")
             return r
 
@@ -900,15 +900,24 @@ def graph_loop(torch, fn, K: int):
 
 
 def call_stats(ms: list, nbytes: int, peak: float) -> dict:
-    """Median / P95 / CV of per-call times, and the median's HBM rate
-    against the copy peak.  "stable" (CV <= 5 %) marks the figures a ratio
-    may be claimed from ("NCCL 专家课程 07", 严格处理不稳定点)."""
+    """Median / P95 / CV of per-call times, and the HBM rate against the copy
+    peak.  "stable" (CV <= 5 %) marks the figures a ratio may be claimed from
+    ("NCCL 专家课程 07", 严格处理不稳定点).  The rate (and every ratio taken
+    from these figures) uses mean_us, the mean of the calls left after the
+    fastest and the slowest tenth are dropped: on the GB300 machines measured
+    here the CUDA event clock advances in steps of 2.048 us, so each call's
+    time is a multiple of that step and a median sits on that grid (up to
+    1 us off, a few per cent of a 30 us call), while the mean over calls
+    that start at varying phases of the clock does not."""
     import numpy as np
-    a = np.asarray(ms, dtype=np.float64)
+    a = np.sort(np.asarray(ms, dtype=np.float64))
     med = float(np.median(a))
-    g = nbytes / (med / 1e3) / 1e9
+    k = a.size // 10
+    t = float(a[k:a.size - k].mean())
+    g = nbytes / (t / 1e3) / 1e9
     cv = float(a.std() / a.mean()) if a.mean() > 0 else 0.0
-    return {"median_us": round(med * 1e3, 2), "p95_us": round(float(np.percentile(a, 95)) * 1e3, 2),
+    return {"median_us": round(med * 1e3, 2), "mean_us": round(t * 1e3, 2),
+            "p95_us": round(float(np.percentile(a, 95)) * 1e3, 2),
             "cv": round(cv, 4), "calls": int(a.size), "bytes": int(nbytes), "gbs": round(g, 1),
             "frac": round(g / peak, 4), "stable": cv <= 0.05}
 
@@ -1208,7 +1217,7 @@ def config_c4(torch, vc, dev, stream, peak, workload_name, args, d=None, memory=
                      "reduce_scatter_only": call_stats(t["reduce_scatter_only"],
                                                        b["reduce_scatter"], peak)},
            "oracle_check": chk.summary(indices=int(idx.size))}
-    med = {k: v["median_us"] for k, v in out["paths"].items()}
+    med = {k: v["mean_us"] for k, v in out["paths"].items()}
     out["rs_then_ag_over_all_reduce"] = (round(med["rs_then_ag"] / med["all_reduce"], 3)
                                          if out["paths"]["all_reduce"]["stable"]
                                          and out["paths"]["rs_then_ag"]["stable"] else "unstable")
@@ -1265,7 +1274,7 @@ def config_c5(torch, vc, dev, stream, peak):
                 row = {"n": n, "bytes_per_rank": nbytes, "dtype": dtype}
                 for key, bk in (("rs", "reduce_scatter"), ("ag", "all_gather"), ("ar", "fused_ar")):
                     st = call_stats(t[key], b[bk], peak)
-                    row[key] = {k: st[k] for k in ("median_us", "p95_us", "cv", "frac")}
+                    row[key] = {k: st[k] for k in ("median_us", "mean_us", "p95_us", "cv", "frac")}
                 row["oracle"] = {"indices": int(idx.size), "mismatches": chk.mismatches}
                 rows.append(row)
                 del d, z, rs, ar, ag
@@ -1299,7 +1308,7 @@ def config_c5(torch, vc, dev, stream, peak):
                 row = {"dtype": dtype, "order": order, "op": op}
                 for key, bk in (("rs", "reduce_scatter"), ("ar", "fused_ar")):
                     st = call_stats(t[key], b[bk], peak)
-                    row[key] = {k: st[k] for k in ("median_us", "cv", "frac")}
+                    row[key] = {k: st[k] for k in ("median_us", "mean_us", "cv", "frac")}
                 row["oracle"] = {"indices": int(idx.size), "mismatches": chk.mismatches}
                 combos.append(row)
         del d, z, y, rs, ar
@@ -1467,8 +1476,9 @@ def run_sweep(args):
     {2, 4, 8, 16, 64}, N * bytes <= 64 GiB) over the four element types: one
     JSON line per point with RS / AG / fused AR GB/s and their fraction of the
     measured copy peak (SUM, the order given by --order).  Inputs are made on
-    the device; each kernel's time is the median of 5 single calls after 3
-    warm-ups.  Before each call a read of twice the L2 evicts the last
+    the device; each kernel's time is the mean of 10 single calls after 3
+    warm-ups, the fastest and the slowest left out (call_stats: the event
+    clock's 2.048 us steps).  Before each call a read of twice the L2 evicts the last
     call's data, and it keeps the GPU busy while the host issues the call:
     the events then time the call on the device, launch latency included,
     without the host's time to reach the launch.  (A write would leave the
@@ -1495,7 +1505,7 @@ def run_sweep(args):
     flush = torch.ones(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
 
-    def t_ms(fn, reps=5):
+    def t_ms(fn, reps=10):
         for _ in range(3):
             fn()
         times = []
@@ -1507,7 +1517,7 @@ def run_sweep(args):
             b.record(stream)
             b.synchronize()
             times.append(a.elapsed_time(b))
-        return sorted(times)[len(times) // 2]
+        return call_stats(times, 1, 1.0)["mean_us"] / 1e3
 
     def sustained(n, M, dtype, dist, kw, d, z, b, set_bytes):
         """Back-to-back calls, the way a training loop issues them: K sets
@@ -1563,7 +1573,8 @@ def run_sweep(args):
             b = step_bytes(n, M, es)
             line = {"sweep": "size_x_ranks", "n": n, "bytes_per_rank": nbytes, "dtype": dtype,
                     "op": args.op, "order": args.order, "peak": peak, "peak_kind": kind,
-                    "timing": "median of 5 single calls, each after an L2-evicting read"}
+                    "timing": "mean of 10 single calls less the fastest and slowest, "
+                              "each after an L2-evicting read"}
             for name, fn, key in (("reduce_scatter", rs, "reduce_scatter"),
                                   ("all_gather", ag, "all_gather"),
                                   ("all_reduce", ar, "fused_ar")):

@@ -158,3 +158,18 @@ def test_check_counts_mismatches_bitwise():
     assert chk.mismatches == 1 and chk.compared == 6
     s = chk.summary(indices=3)
     assert not s["bit_exact"] and s["indices"] == 3 and s["outputs"] == ["x"]
+
+
+def test_call_stats_rate_survives_a_coarse_event_clock():
+    """A 29.5 us call read by an event clock that advances in 2.048 us
+    steps: four readings of ten land on 30.72 us, six on 28.672 us.  The
+    median sits on the grid; the rate comes from the mean of the middle
+    eight, which stays within the step's tenth of the true time, and one
+    slow outlier does not move it."""
+    ms = [0.028672] * 6 + [0.03072] * 4
+    st = bench.call_stats(ms, 1_000_000, 1.0)
+    assert st["median_us"] == 28.67
+    assert abs(st["mean_us"] - 29.5) < 0.2
+    assert abs(st["gbs"] - 1e6 / 29.44e-6 / 1e9) < 0.1
+    slow = ms[:-1] + [0.060]
+    assert bench.call_stats(slow, 1_000_000, 1.0)["mean_us"] == st["mean_us"]
