@@ -168,10 +168,11 @@ __host__ __device__ __forceinline__ uint4 ld16(const void* p) {
 __host__ __device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // A 16-byte store with the evict-first streaming hint, for the AllGather's
-// N output streams.  Measured on GB300 (back-to-back calls): 0.3-0.7 % of
-// the copy rate at 4 x 256 MiB and 8 x 1 GiB, and the decomposed AllReduce
-// of a 25 MiB bf16 bucket on 8 ranks 0.93x -> 0.94x (the gather's own
-// writes leave L2 first, so the shards the ReduceScatter just wrote stay).
+// N output streams (N >= 4).  Measured on GB300 (back-to-back calls): 0.3-1 %
+// of the copy rate at 4 x 256 MiB, 8 x 64 MiB and 8 x 1 GiB, and the
+// decomposed AllReduce of a 25 MiB bf16 bucket on 8 ranks 0.93x -> 0.94x
+// (the gather's own writes leave L2 first, so the shards the ReduceScatter
+// just wrote stay).
 __device__ __forceinline__ void st16_stream(void* p, uint4 v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
@@ -1444,10 +1445,21 @@ __global__ void __launch_bounds__(kThreads) vc_ag_kernel(const __grid_constant__
                 for (int u = 0; u < S; ++u)
                     val[u] = gather_load<ES>(p, s, (v0 + (long long)u * blockDim.x) * V);
             }
-            for (int r = r0; r < r1; ++r) {
-                U* dst = static_cast<U*>(p.out[r]) + v0 * V;
+            // streaming stores from four outputs on (st16_stream); below
+            // that they measured slower (3 ranks: bf16 with shards off the
+            // grid 0.92x -> 0.88x of the copy peak, fp32 0.998x -> 0.992x)
+            if (r1 - r0 >= 4) {
+                for (int r = r0; r < r1; ++r) {
+                    U* dst = static_cast<U*>(p.out[r]) + v0 * V;
 #pragma unroll
-                for (int u = 0; u < S; ++u) st16_stream(dst + (long long)u * blockDim.x * V, val[u]);
+                    for (int u = 0; u < S; ++u) st16_stream(dst + (long long)u * blockDim.x * V, val[u]);
+                }
+            } else {
+                for (int r = r0; r < r1; ++r) {
+                    U* dst = static_cast<U*>(p.out[r]) + v0 * V;
+#pragma unroll
+                    for (int u = 0; u < S; ++u) st16(dst + (long long)u * blockDim.x * V, val[u]);
+                }
             }
         } else {
 #pragma unroll 1
