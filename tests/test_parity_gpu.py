@@ -567,6 +567,27 @@ def test_in_place_straddling_vectors(env, dtype):
 ESIZE = {"int32": 4, "int64": 8, "float32": 4, "bfloat16": 2}
 
 
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int64"])
+def test_partial_last_span(env, dtype):
+    """The reduction kernels with the operands preloaded (N <= 8) give a
+    thread U vectors (four up to four ranks, two up to eight) in each span of
+    256 x U vectors, and take the last span of the index space first; there
+    a thread may own only its first k < U vectors.  Shapes whose vector count
+    is a whole number of spans, one vector short of it, one past it, and one
+    element short, on 3 and 8 ranks, every order, SUM and MAX, all paths
+    against the oracle."""
+    V = 16 // ESIZE[dtype]
+    for n, U in ((3, 4), (8, 2)):
+        span = 256 * U
+        for nv, extra in ((3 * span, 0), (3 * span - 1, 0), (3 * span + 1, 0), (3 * span, -1)):
+            M = nv * V + extra
+            for order in orders_for(n):
+                for op in ("sum", "max"):
+                    xs = gen(dtype, n, M, seed=M + n)
+                    res = run_all_paths(env, xs, dtype, op, order)
+                    check_all_paths(res, xs, dtype, op, order, tag=f"N={n} M={M}")
+
+
 @pytest.mark.parametrize("dtype", SWEEP_DTYPES)
 def test_shards_off_the_vector_grid(env, dtype):
     """When q elements are not a whole number of 16-byte vectors, shard c
