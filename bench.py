@@ -37,7 +37,9 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU
 time is the max over ranks, and value counts the bytes of all ranks.  The
 ranks talk only over a host-side gloo group (a barrier, a max and a sum).
 --impl reference times the CPU oracle instead, on a bounded window of the
-same workload (rank 0 only).
+same workload (rank 0 only).  Single cases for profiling: --one (one
+collective on one shape), --bucket-path (one gradient-bucket collective),
+--sweep (the size x rank-count sweep).
 """
 from __future__ import annotations
 
@@ -1641,6 +1643,47 @@ def run_one(args):
     return 0
 
 
+def run_bucket_path(args):
+    """One gradient-bucket collective over the transformer-shaped set of
+    bucket_report (145 bf16 tensors, 351 MiB per rank, 8 ranks), W warm-up
+    calls then K timed, one launch per bucket each: the case a single-kernel
+    profile of the bucket kernels captures.  --bucket-path PATH, PATH in
+    ar_fused, ar_views, rs_fused, rs_views, ag_fused.  Prints one JSON line."""
+    import torch
+
+    import allreduce_reducescatter_allgather_gb300 as vc  # noqa: F401 (loads the library)
+    from allreduce_reducescatter_allgather_gb300 import bucketing
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = 8
+    shapes = transformer_grad_shapes()
+    gb = bucketing.GradientBuckets(shapes, torch.bfloat16, n, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(99)
+    grads = [[torch.randn(s, generator=g, device=dev).to(torch.bfloat16) for s in shapes]
+             for _ in range(n)]
+    gb.bind(grads)
+    gb.reduce_scatter(op=args.op, order=args.order)  # the shards the AllGather reads
+    fn = {"ar_fused": lambda: gb.all_reduce_tensors(op=args.op, order=args.order, fused=True),
+          "ar_views": lambda: gb.all_reduce(op=args.op, order=args.order),
+          "rs_fused": lambda: gb.reduce_scatter_tensors(op=args.op, order=args.order, fused=True),
+          "rs_views": lambda: gb.reduce_scatter(op=args.op, order=args.order),
+          "ag_fused": lambda: gb.all_gather_tensors()}[args.bucket_path]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"bucket_path": args.bucket_path, "buckets": len(gb.buckets),
+                      "bucket_counts": [bk.count for bk in gb.buckets], "calls": args.steps,
+                      "us_per_call": round(a.elapsed_time(b) / args.steps * 1e3, 1)}), flush=True)
+    return 0
+
+
 def main(argv=None):
     import synthetic_inputs as si
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -1669,6 +1712,9 @@ def main(argv=None):
     ap.add_argument("--one", default="",
                     help="time one collective instead: PATH:DTYPE:N:ELEMENTS, e.g. "
                          "rs:bfloat16:12:8388608 (PATH in rs, ag, ar, dec)")
+    ap.add_argument("--bucket-path", default="",
+                    choices=["", "ar_fused", "ar_views", "rs_fused", "rs_views", "ag_fused"],
+                    help="time one gradient-bucket collective over the 145-tensor set instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -1677,9 +1723,11 @@ def main(argv=None):
         workload["M"] = args.elements
     if args.impl == "reference":
         return run_reference(args, workload)
-    if args.sweep or args.one:
+    if args.sweep or args.one or args.bucket_path:
         import __graft_entry__
         __graft_entry__.build()
+        if args.bucket_path:
+            return run_bucket_path(args)
         return run_sweep(args) if args.sweep else run_one(args)
     if dist_info()[0] == 1:
         import __graft_entry__
