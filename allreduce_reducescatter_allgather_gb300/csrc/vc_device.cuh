@@ -1314,10 +1314,16 @@ __device__ __forceinline__ void reduce_body(const ReduceParams& p) {
 // spills.  The ReduceScatter, which reads N streams per store, gains from
 // the extra warps' loads in flight: measured 0.5-1.5 points of the copy peak
 // (N = 8 1.046x -> 1.052x, the 25 MiB bucket on 8 ranks 0.982x -> 0.993x);
-// the AllReduce and the fp32 ReduceScatter gained nothing.
+// the AllReduce and the fp32 ReduceScatter gained nothing.  At N = 2 the
+// same ReduceScatter asks for four (62 registers instead of 65-72, which
+// left three): 2 x 64 MiB 0.97x -> 0.99x, with shards off the grid 0.90x
+// -> 0.94x, 2 x 128 MiB 1.03x -> 1.02x; the fp32 kernel already runs four.
 template <int NT, bool RS = false, int ES = 4>
 constexpr int min_blocks() {
-    return NT > 0 ? ((RS && ES == 2 && NT >= 4 && NT <= 8) ? 3 : 1) : 2;
+    if (NT <= 0) return 2;
+    if (RS && ES == 2 && NT >= 4 && NT <= 8) return 3;
+    if (RS && ES == 2 && NT == 2) return 4;
+    return 1;
 }
 
 // ReduceScatter: index space [0, N*q), one store per element into the shard
